@@ -1,0 +1,176 @@
+"""CPU oracle for the in-place partial interleaved rotary embedding.
+
+TEST INFRASTRUCTURE, NOT PRODUCT CODE.  Only ``tests/``,
+``__graft_entry__.smoke()`` and the CPU-baseline leg of ``bench.py`` may
+import this package.  It shares no code with the CUDA path, and the CUDA path
+never imports it.
+
+Contents
+--------
+* ``rope_oracle.c`` -- the scalar C statement of the forward and backward
+  (gather-chain and pair-rotation formulations) and the IEEE 754 storage
+  conversions, built into ``librope_oracle.so`` by :func:`build`.
+* ``rope_mil.py`` -- a third, array-level formulation (reshape / slice /
+  negate / concat), written with numpy float32 operations.
+
+Sources: "CANN ops-transformer inplace_partial_rotary_mul" (formula section
+and its kernel op chain; tiling section for FP32 compute with CAST_RINT);
+"ANE实战 RoPE位置编码在MIL中的纯ANE实现" (rotate_half lowering table, backward
+section).
+
+Parity status: every function here is pinned by ``tests/test_oracle_*.py``
+(closed forms, special cases, invariants, brute-force Jacobians, library
+conversions and a hand-worked example); none is "parity unpinned".
+"""
+from __future__ import annotations
+
+import contextlib
+import ctypes
+import os
+import subprocess
+
+import numpy as np
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+SRC = os.path.join(HERE, "rope_oracle.c")
+LIB = os.path.join(HERE, "librope_oracle.so")
+
+BF16, FP16, FP32 = 0, 1, 2
+DTYPE_CODES = {"bf16": BF16, "fp16": FP16, "fp32": FP32}
+GATHER_CHAIN, PAIR_ROTATION = 0, 1
+FWD, BWD = 0, 1
+
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    """Compile the oracle with gcc (no FMA contraction, no fast-math)."""
+    if force or not os.path.exists(LIB) or os.path.getmtime(LIB) < os.path.getmtime(SRC):
+        cmd = ["gcc", "-O2", "-std=c11", "-ffp-contract=off", "-fno-fast-math",
+               "-fPIC", "-shared", "-o", LIB, SRC, "-lm"]
+        subprocess.run(cmd, check=True)
+    return LIB
+
+
+def _open(path):
+    lib = ctypes.CDLL(path)
+    i64p = ctypes.POINTER(ctypes.c_int64)
+    lib.oracle_rope.restype = ctypes.c_int
+    lib.oracle_rope.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_void_p,
+                                ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64,
+                                ctypes.c_int64, ctypes.c_int64, ctypes.c_int64,
+                                i64p, i64p, i64p, i64p, ctypes.c_int64, ctypes.c_int64]
+    for name in ("oracle_f32_to_bf16_n", "oracle_f32_to_f16_n",
+                 "oracle_bf16_to_f32_n", "oracle_f16_to_f32_n"):
+        fn = getattr(lib, name)
+        fn.restype = None
+        fn.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64]
+    return lib
+
+
+def _load():
+    global _lib
+    if _lib is None:
+        build()
+        _lib = _open(LIB)
+    return _lib
+
+
+@contextlib.contextmanager
+def using_library(path: str):
+    """Temporarily route every oracle call through another build of the
+    oracle source (the mutation tests use this to run the pins against
+    deliberately broken copies)."""
+    global _lib
+    saved = _load()
+    _lib = _open(path)
+    try:
+        yield
+    finally:
+        _lib = saved
+
+
+def _i64x4(vals):
+    return (ctypes.c_int64 * 4)(*[int(v) for v in vals])
+
+
+def _elem_strides(arr: np.ndarray):
+    return [s // arr.itemsize for s in arr.strides]
+
+
+def rope(direction: int, x: np.ndarray, r1: np.ndarray, r2: np.ndarray, dtype: str,
+         start: int, end: int, formulation: int = GATHER_CHAIN) -> np.ndarray:
+    """Return a copy of ``x`` with the forward (``FWD``) or backward (``BWD``)
+    applied to lanes ``[start, end)`` of its last axis.
+
+    ``x`` is a contiguous 4-D array (B, S, N, D) holding the storage type:
+    float32 for ``fp32``, uint16 bit patterns for ``bf16`` and ``fp16``.
+    ``r1`` (cos) and ``r2`` (sin) are 4-D arrays of the same storage type that
+    broadcast against the slice; they may be strided views (numpy strides in
+    bytes are converted to element strides).
+    """
+    lib = _load()
+    code = DTYPE_CODES[dtype]
+    want = np.float32 if code == FP32 else np.uint16
+    for a in (x, r1, r2):
+        if a.dtype != want or a.ndim != 4:
+            raise ValueError(f"oracle expects 4-D {want} arrays for {dtype}")
+    out = np.ascontiguousarray(x).copy()
+    B, S, N, D = out.shape
+    rc = lib.oracle_rope(direction, formulation, code,
+                         out.ctypes.data, r1.ctypes.data, r2.ctypes.data, B, S, N, D,
+                         _i64x4(r1.shape), _i64x4(_elem_strides(r1)),
+                         _i64x4(r2.shape), _i64x4(_elem_strides(r2)), start, end)
+    if rc != 0:
+        raise ValueError("oracle rejected the arguments")
+    return out
+
+
+def fwd(x, r1, r2, dtype, start, end, formulation=GATHER_CHAIN):
+    return rope(FWD, x, r1, r2, dtype, start, end, formulation)
+
+
+def bwd(g, r1, r2, dtype, start, end, formulation=GATHER_CHAIN):
+    return rope(BWD, g, r1, r2, dtype, start, end, formulation)
+
+
+def f32_to_bf16(a: np.ndarray) -> np.ndarray:
+    a = np.ascontiguousarray(a, dtype=np.float32)
+    out = np.empty(a.shape, np.uint16)
+    _load().oracle_f32_to_bf16_n(a.ctypes.data, out.ctypes.data, a.size)
+    return out
+
+
+def f32_to_f16(a: np.ndarray) -> np.ndarray:
+    a = np.ascontiguousarray(a, dtype=np.float32)
+    out = np.empty(a.shape, np.uint16)
+    _load().oracle_f32_to_f16_n(a.ctypes.data, out.ctypes.data, a.size)
+    return out
+
+
+def bf16_to_f32(h: np.ndarray) -> np.ndarray:
+    h = np.ascontiguousarray(h, dtype=np.uint16)
+    out = np.empty(h.shape, np.float32)
+    _load().oracle_bf16_to_f32_n(h.ctypes.data, out.ctypes.data, h.size)
+    return out
+
+
+def f16_to_f32(h: np.ndarray) -> np.ndarray:
+    h = np.ascontiguousarray(h, dtype=np.uint16)
+    out = np.empty(h.shape, np.float32)
+    _load().oracle_f16_to_f32_n(h.ctypes.data, out.ctypes.data, h.size)
+    return out
+
+
+def widen(a: np.ndarray, dtype: str) -> np.ndarray:
+    """Storage array -> float32 values, through the oracle's own conversions."""
+    if dtype == "fp32":
+        return np.asarray(a, np.float32)
+    return bf16_to_f32(a) if dtype == "bf16" else f16_to_f32(a)
+
+
+def narrow(a: np.ndarray, dtype: str) -> np.ndarray:
+    """float32 values -> storage array, through the oracle's own RNE rounding."""
+    if dtype == "fp32":
+        return np.asarray(a, np.float32)
+    return f32_to_bf16(a) if dtype == "bf16" else f32_to_f16(a)
