@@ -1,0 +1,155 @@
+/*
+ * rope_partial.h -- C ABI of the GB300 in-place partial interleaved rotary
+ * position embedding (inplace_partial_rotary_mul, forward and backward).
+ *
+ * Operation ("CANN ops-transformer inplace_partial_rotary_mul",
+ * mhpn.cn/news/2302710, section 功能与计算公式): x is a contiguous tensor of
+ * shape (B, S, N, D) ("BSND": batch, sequence, heads, head dim).  Only the
+ * lanes [start, end) of its last axis change.  With L = end - start and the
+ * lanes counted from start, each pair (2i, 2i+1) of the slice becomes
+ *
+ *     y[2i]   = x[2i]   * c[2i]   - x[2i+1] * s[2i]
+ *     y[2i+1] = x[2i+1] * c[2i+1] + x[2i]   * s[2i+1]
+ *
+ * i.e. x_out = x_slice * cos + x_rotate * sin, where x_rotate swaps each pair
+ * (the XOR-1 gather) and negates its even lanes; c comes from r1 (cos) and
+ * s from r2 (sin).  The result is written back into x.
+ *
+ * The backward applies the transposed rotation to the incoming gradient g,
+ * in place (same page, section 自动微分说明; the inverse rotation of
+ * "ANE实战 RoPE位置编码在MIL中的纯ANE实现", section 反向传播):
+ *
+ *     dx[2i]   = g[2i]   * c[2i]   + g[2i+1] * s[2i+1]
+ *     dx[2i+1] = g[2i+1] * c[2i+1] - g[2i]   * s[2i]
+ *
+ * Arithmetic: every input is widened to fp32; each product is one fp32
+ * rounding and the sum is one fp32 rounding (no fused multiply-add); the
+ * result is rounded once to the storage type, round-to-nearest-even (the
+ * CAST_RINT write-back of the page's tiling section).  Results are
+ * deterministic: no atomics, no reductions.
+ *
+ * Memory: every pointer is a device pointer (or managed memory) on the
+ * current CUDA device.  The caller owns every buffer; the library allocates
+ * nothing and needs no workspace.  Calls are asynchronous on `stream` and
+ * never synchronise.
+ *
+ * Error behaviour: arguments are validated on the host before anything is
+ * launched; an invalid call changes nothing and returns an error status.
+ * A call whose work is empty (end == start, or any of B, S, N, D is 0)
+ * returns ROPE_OK without a launch and then accepts null data pointers
+ * (the page's no-op rule for an empty slice or empty tensor).
+ * rope_last_error_message() describes the most recent failure on the
+ * calling thread.
+ */
+#ifndef ROPE_PARTIAL_H
+#define ROPE_PARTIAL_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* The same type as cudaStream_t (a CUDA runtime stream handle); 0 is the
+   legacy default stream. */
+typedef struct CUstream_st* rope_stream_t;
+
+/* Storage types of x, r1 and r2 (the three the page registers). */
+typedef enum {
+    ROPE_BF16 = 0,
+    ROPE_FP16 = 1,
+    ROPE_FP32 = 2
+} rope_dtype_t;
+
+/* Status codes (split after the aclnn null-pointer / invalid-parameter /
+   internal-error convention). */
+typedef enum {
+    ROPE_OK = 0,
+    ROPE_ERR_NULLPTR = 1, /* a required pointer is null                       */
+    ROPE_ERR_INVALID = 2, /* dtype, sizes, slice, broadcast, stride or align   */
+    ROPE_ERR_CUDA = 3     /* the launch or a device query failed               */
+} rope_status_t;
+
+/*
+ * rope_partial_inplace_fwd -- rotate x[..., start:end) in place.
+ *
+ *   x          device pointer to a contiguous (B, S, N, D) tensor of `dtype`,
+ *              read and written.  Aligned to its element size.
+ *   r1, r2     device pointers to cos and sin: 4-D tensors of `dtype` with
+ *              shape rX_shape[0..3] and ELEMENT strides rX_stride[0..3].
+ *              Each of rX_shape[0..2] is 1 (broadcast; its stride is then
+ *              ignored) or equal to B, S, N respectively; rX_shape[3] == L.
+ *              rX_stride[3] must be 1 and the other strides >= 0.  r1 and r2
+ *              are only read and must not overlap x.
+ *   B, S, N, D sizes of x, each >= 0; D even and D <= 1024.
+ *   start, end 0 <= start <= end <= D and L = end - start even.  start may be
+ *              odd: pairs are counted from start.
+ *   stream     the CUDA stream to launch on.
+ *
+ * Returns ROPE_OK after the launch was queued (or for an empty call),
+ * ROPE_ERR_NULLPTR for a null x / r1 / r2 / shape / stride pointer when
+ * there is work, ROPE_ERR_INVALID when a rule above is broken, and
+ * ROPE_ERR_CUDA when the launch fails.
+ */
+rope_status_t rope_partial_inplace_fwd(void* x, const void* r1, const void* r2,
+                                       rope_dtype_t dtype, int64_t B, int64_t S,
+                                       int64_t N, int64_t D,
+                                       const int64_t r1_shape[4], const int64_t r1_stride[4],
+                                       const int64_t r2_shape[4], const int64_t r2_stride[4],
+                                       int64_t start, int64_t end, rope_stream_t stream);
+
+/*
+ * rope_partial_inplace_bwd -- overwrite grad[..., start:end) with the
+ * gradient with respect to x of the forward above (the transposed rotation).
+ * Arguments, layout, ownership and errors are those of the forward, with
+ * `grad` (the incoming gradient, shape (B, S, N, D)) in place of x.  r1 and
+ * r2 get no gradient.
+ */
+rope_status_t rope_partial_inplace_bwd(void* grad, const void* r1, const void* r2,
+                                       rope_dtype_t dtype, int64_t B, int64_t S,
+                                       int64_t N, int64_t D,
+                                       const int64_t r1_shape[4], const int64_t r1_stride[4],
+                                       const int64_t r2_shape[4], const int64_t r2_stride[4],
+                                       int64_t start, int64_t end, rope_stream_t stream);
+
+/* A static, human-readable name of a status code. */
+const char* rope_status_str(rope_status_t status);
+
+/* A description of the most recent non-OK status returned on the calling
+   thread ("" if none).  The string stays valid until the thread's next call. */
+const char* rope_last_error_message(void);
+
+/*
+ * Launch plan, for inspection and tests.  rope_partial_plan validates the
+ * same arguments as the forward (data pointers are used only for their
+ * alignment and may be any value with the alignment they will have) and
+ * reports the kernel the call would launch.  sm_count > 0 sizes the grid
+ * for that many SMs without touching the GPU; sm_count == 0 asks the current
+ * device.  No kernel is launched.
+ */
+typedef struct {
+    int32_t path;             /* 0: no launch (empty), 1: vector kernel, 2: scalar-pair kernel */
+    int32_t vec_bytes;        /* bytes per global access of x on the vector path (16, 8 or 4)  */
+    int32_t heads_per_thread; /* heads one thread walks with its cos/sin kept in registers     */
+    int32_t threads_per_block;
+    int64_t blocks;           /* grid size                                                    */
+    int64_t tasks;            /* (token, head group, chunk) work items                        */
+    int32_t chunks_per_row;   /* accesses covering one row's slice                            */
+    int32_t r_per_head;       /* 1 when cos/sin differ between heads (reloaded per head)       */
+    int64_t launches;         /* kernel launches: calls whose work index would pass 2^31 are   */
+                              /* split into launches over whole batches or runs of tokens       */
+} rope_plan_t;
+
+rope_status_t rope_partial_plan(const void* x, const void* r1, const void* r2,
+                                rope_dtype_t dtype, int64_t B, int64_t S, int64_t N, int64_t D,
+                                const int64_t r1_shape[4], const int64_t r1_stride[4],
+                                const int64_t r2_shape[4], const int64_t r2_stride[4],
+                                int64_t start, int64_t end, int32_t sm_count,
+                                rope_plan_t* plan);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* ROPE_PARTIAL_H */

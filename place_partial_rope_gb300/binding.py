@@ -1,0 +1,148 @@
+"""ctypes binding of ``librope_partial.so`` (C ABI: ``include/rope_partial.h``).
+
+Argument marshalling only: every step of the operation runs in the library's
+CUDA kernels.  PyTorch supplies device memory and the current stream.  If the
+library has not been built, loading raises -- there is no CPU fallback.
+
+    rope_partial_inplace_fwd(x, r1, r2, start, end, stream=None)
+    rope_partial_inplace_bwd(grad, r1, r2, start, end, stream=None)
+
+``x`` / ``grad``: contiguous CUDA tensor (B, S, N, D) of bf16, fp16 or fp32,
+modified in place.  ``r1`` (cos) and ``r2`` (sin): 4-D CUDA tensors of the
+same dtype and device that broadcast against ``x[..., start:end]`` (any
+strides with a contiguous last dim; size-1 dims broadcast).  Both calls are
+asynchronous on ``stream`` (default: torch's current stream of x's device).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+_LIB_PATH = os.path.join(_PKG, "librope_partial.so")
+
+ROPE_OK, ROPE_ERR_NULLPTR, ROPE_ERR_INVALID, ROPE_ERR_CUDA = 0, 1, 2, 3
+ROPE_BF16, ROPE_FP16, ROPE_FP32 = 0, 1, 2
+DTYPE_CODE = {torch.bfloat16: ROPE_BF16, torch.float16: ROPE_FP16, torch.float32: ROPE_FP32}
+
+_lib = None
+
+
+class RopePlan(ctypes.Structure):
+    """Mirror of ``rope_plan_t``."""
+    _fields_ = [("path", ctypes.c_int32), ("vec_bytes", ctypes.c_int32),
+                ("heads_per_thread", ctypes.c_int32), ("threads_per_block", ctypes.c_int32),
+                ("blocks", ctypes.c_int64), ("tasks", ctypes.c_int64),
+                ("chunks_per_row", ctypes.c_int32), ("r_per_head", ctypes.c_int32),
+                ("launches", ctypes.c_int64)]
+
+
+class RopeError(RuntimeError):
+    def __init__(self, status: int, message: str):
+        super().__init__(message)
+        self.status = status
+
+
+def library_path() -> str:
+    return _LIB_PATH
+
+
+def load_library() -> ctypes.CDLL:
+    """Load the CUDA library once; raise if it is missing (no fallback)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(_LIB_PATH):
+        raise RuntimeError(
+            f"{_LIB_PATH} is not built; build it with `python -m place_partial_rope_gb300.build` "
+            "(needs nvcc). There is no CPU fallback.")
+    lib = ctypes.CDLL(_LIB_PATH)
+    i64p = ctypes.POINTER(ctypes.c_int64)
+    args = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int, ctypes.c_int64,
+            ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, i64p, i64p, i64p, i64p,
+            ctypes.c_int64, ctypes.c_int64]
+    for name in ("rope_partial_inplace_fwd", "rope_partial_inplace_bwd"):
+        fn = getattr(lib, name)
+        fn.restype = ctypes.c_int
+        fn.argtypes = args + [ctypes.c_void_p]
+    lib.rope_partial_plan.restype = ctypes.c_int
+    lib.rope_partial_plan.argtypes = args + [ctypes.c_int32, ctypes.POINTER(RopePlan)]
+    lib.rope_status_str.restype = ctypes.c_char_p
+    lib.rope_status_str.argtypes = [ctypes.c_int]
+    lib.rope_last_error_message.restype = ctypes.c_char_p
+    lib.rope_last_error_message.argtypes = []
+    _lib = lib
+    return lib
+
+
+def _i64x4(vals):
+    return (ctypes.c_int64 * 4)(*[int(v) for v in vals])
+
+
+def _raise_for(lib, status: int):
+    if status != ROPE_OK:
+        name = lib.rope_status_str(status).decode()
+        msg = lib.rope_last_error_message().decode()
+        raise RopeError(status, f"{name}: {msg}")
+
+
+def _stream_handle(stream, device) -> int:
+    if stream is None:
+        return torch.cuda.current_stream(device).cuda_stream
+    if isinstance(stream, torch.cuda.Stream):
+        return stream.cuda_stream
+    return int(stream)
+
+
+def _marshal(x: torch.Tensor, r1: torch.Tensor, r2: torch.Tensor):
+    if x.dim() != 4:
+        raise RopeError(ROPE_ERR_INVALID, f"x must be 4-D (B, S, N, D), got {x.dim()}-D")
+    if r1.dim() != 4 or r2.dim() != 4:
+        raise RopeError(ROPE_ERR_INVALID, "r1 and r2 must be 4-D")
+    if x.dtype not in DTYPE_CODE:
+        raise RopeError(ROPE_ERR_INVALID, f"unsupported dtype {x.dtype}")
+    if r1.dtype != x.dtype or r2.dtype != x.dtype:
+        raise RopeError(ROPE_ERR_INVALID, "r1, r2 and x must share one dtype")
+    if not x.is_contiguous():
+        raise RopeError(ROPE_ERR_INVALID, "x must be contiguous")
+    for t in (x, r1, r2):
+        if not t.is_cuda or t.device != x.device:
+            raise RopeError(ROPE_ERR_INVALID, "x, r1 and r2 must be CUDA tensors on one device")
+    return (x.data_ptr(), r1.data_ptr(), r2.data_ptr(), DTYPE_CODE[x.dtype], *x.shape,
+            _i64x4(r1.shape), _i64x4(r1.stride()), _i64x4(r2.shape), _i64x4(r2.stride()))
+
+
+def _call(name: str, x, r1, r2, start: int, end: int, stream=None) -> None:
+    lib = load_library()
+    margs = _marshal(x, r1, r2)
+    with torch.cuda.device(x.device):
+        st = getattr(lib, name)(*margs, int(start), int(end), _stream_handle(stream, x.device))
+    _raise_for(lib, st)
+
+
+def rope_partial_inplace_fwd(x: torch.Tensor, r1: torch.Tensor, r2: torch.Tensor, start: int,
+                             end: int, stream=None) -> None:
+    """Rotate ``x[..., start:end]`` in place (forward)."""
+    _call("rope_partial_inplace_fwd", x, r1, r2, start, end, stream)
+
+
+def rope_partial_inplace_bwd(grad: torch.Tensor, r1: torch.Tensor, r2: torch.Tensor, start: int,
+                             end: int, stream=None) -> None:
+    """Overwrite ``grad[..., start:end]`` with the transposed rotation (backward)."""
+    _call("rope_partial_inplace_bwd", grad, r1, r2, start, end, stream)
+
+
+def rope_partial_plan(x: torch.Tensor, r1: torch.Tensor, r2: torch.Tensor, start: int, end: int,
+                      sm_count: int = 0) -> RopePlan:
+    """The launch plan the forward would use (no launch).  Works on CPU
+    tensors as well when ``sm_count`` > 0, since only shapes, strides and
+    pointer alignment are read."""
+    lib = load_library()
+    plan = RopePlan()
+    args = (x.data_ptr(), r1.data_ptr(), r2.data_ptr(), DTYPE_CODE[x.dtype], *x.shape,
+            _i64x4(r1.shape), _i64x4(r1.stride()), _i64x4(r2.shape), _i64x4(r2.stride()))
+    st = lib.rope_partial_plan(*args, int(start), int(end), int(sm_count), ctypes.byref(plan))
+    _raise_for(lib, st)
+    return plan

@@ -1,0 +1,339 @@
+// rope_host.cpp -- the C ABI entry points of include/rope_partial.h.
+//
+// Everything here is host logic: argument validation (the constraint list of
+// "CANN ops-transformer inplace_partial_rotary_mul", section 约束说明),
+// broadcast-stride resolution for cos/sin, the empty-call rule (section
+// 功能与计算公式: start == end leaves x unchanged; the backward accepts empty
+// tensors), the choice of kernel path and access width, grid sizing, and the
+// split of very large calls into launches whose flat work index fits 32 bits.
+// No CUDA call is made before the arguments have been validated, and none
+// at all for a rejected or empty call.
+#include <stdarg.h>
+#include <stdint.h>
+#include <stdio.h>
+
+#include "rope_internal.h"
+
+namespace rope {
+namespace {
+
+thread_local char g_msg[512] = "";
+
+rope_status_t fail(rope_status_t st, const char* fmt, ...) {
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(g_msg, sizeof(g_msg), fmt, ap);
+    va_end(ap);
+    return st;
+}
+
+int elem_bytes(int dtype) { return dtype == ROPE_FP32 ? 4 : 2; }
+
+struct Resolved {
+    int e = 0;
+    int64_t L = 0;
+    bool empty = false;
+    int64_t rb[2][3] = {{0, 0, 0}, {0, 0, 0}};  // byte strides (b, s, n); 0 on broadcast dims
+};
+
+bool mul_overflows(int64_t a, int64_t b) { return a != 0 && b > INT64_MAX / a; }
+
+rope_status_t check(const void* x, const void* r1, const void* r2, int dtype, int64_t B,
+                    int64_t S, int64_t N, int64_t D, const int64_t* r1_shape,
+                    const int64_t* r1_stride, const int64_t* r2_shape, const int64_t* r2_stride,
+                    int64_t start, int64_t end, Resolved* out) {
+    if (dtype != ROPE_BF16 && dtype != ROPE_FP16 && dtype != ROPE_FP32)
+        return fail(ROPE_ERR_INVALID, "dtype %d is not bf16 (0), fp16 (1) or fp32 (2)", dtype);
+    if (B < 0 || S < 0 || N < 0 || D < 0)
+        return fail(ROPE_ERR_INVALID, "negative size: B=%lld S=%lld N=%lld D=%lld", (long long)B,
+                    (long long)S, (long long)N, (long long)D);
+    if (D % 2 != 0) return fail(ROPE_ERR_INVALID, "head dim D=%lld must be even", (long long)D);
+    if (D > 1024) return fail(ROPE_ERR_INVALID, "head dim D=%lld exceeds 1024", (long long)D);
+    if (start < 0 || end < start || end > D)
+        return fail(ROPE_ERR_INVALID, "partial slice [%lld, %lld) must satisfy 0 <= start <= end <= D=%lld",
+                    (long long)start, (long long)end, (long long)D);
+    const int64_t L = end - start;
+    if (L % 2 != 0)
+        return fail(ROPE_ERR_INVALID, "slice length end - start = %lld must be even", (long long)L);
+
+    const bool empty = L == 0 || B == 0 || S == 0 || N == 0 || D == 0;
+    const int64_t xdim[3] = {B, S, N};
+    const int64_t* shapes[2] = {r1_shape, r2_shape};
+    const int64_t* strides[2] = {r1_stride, r2_stride};
+    for (int r = 0; r < 2; ++r) {
+        if (!shapes[r]) {
+            if (empty) continue;
+            return fail(ROPE_ERR_NULLPTR, "r%d_shape is null", r + 1);
+        }
+        for (int k = 0; k < 3; ++k)
+            if (!(shapes[r][k] == 1 || shapes[r][k] == xdim[k]))
+                return fail(ROPE_ERR_INVALID, "r%d dim %d is %lld; it must be 1 or %lld to broadcast",
+                            r + 1, k, (long long)shapes[r][k], (long long)xdim[k]);
+        if (shapes[r][3] != L)
+            return fail(ROPE_ERR_INVALID, "r%d last dim is %lld; it must equal end - start = %lld",
+                        r + 1, (long long)shapes[r][3], (long long)L);
+    }
+    out->L = L;
+    out->e = elem_bytes(dtype);
+    if (empty) {
+        out->empty = true;
+        return ROPE_OK;
+    }
+
+    if (!x) return fail(ROPE_ERR_NULLPTR, "x is null");
+    if (!r1) return fail(ROPE_ERR_NULLPTR, "r1 (cos) is null");
+    if (!r2) return fail(ROPE_ERR_NULLPTR, "r2 (sin) is null");
+    const int e = out->e;
+    int64_t total = B;
+    if (mul_overflows(total, S) || mul_overflows(total * S, N) || mul_overflows(total * S * N, D) ||
+        mul_overflows(total * S * N * D, e))
+        return fail(ROPE_ERR_INVALID, "x of %lld x %lld x %lld x %lld elements overflows 64-bit bytes",
+                    (long long)B, (long long)S, (long long)N, (long long)D);
+    for (int r = 0; r < 2; ++r) {
+        if (!strides[r]) return fail(ROPE_ERR_NULLPTR, "r%d_stride is null", r + 1);
+        if (L > 1 && strides[r][3] != 1)
+            return fail(ROPE_ERR_INVALID, "r%d last-dim stride is %lld; it must be 1 (contiguous)",
+                        r + 1, (long long)strides[r][3]);
+        for (int k = 0; k < 3; ++k) {
+            if (shapes[r][k] == 1) {
+                out->rb[r][k] = 0;
+                continue;
+            }
+            if (strides[r][k] < 0)
+                return fail(ROPE_ERR_INVALID, "r%d stride %d is negative (%lld)", r + 1, k,
+                            (long long)strides[r][k]);
+            if (mul_overflows(strides[r][k], shapes[r][k] * e))
+                return fail(ROPE_ERR_INVALID, "r%d stride %d overflows", r + 1, k);
+            out->rb[r][k] = strides[r][k] * e;
+        }
+    }
+    if (reinterpret_cast<uintptr_t>(x) % e || reinterpret_cast<uintptr_t>(r1) % e ||
+        reinterpret_cast<uintptr_t>(r2) % e)
+        return fail(ROPE_ERR_INVALID, "x, r1 and r2 must be aligned to their %d-byte elements", e);
+    return ROPE_OK;
+}
+
+// Heads per thread: the largest power of two U <= min(cap, N) whose
+// ceil(N / U) * U head slots leave at most a quarter idle.  An idle slot
+// costs issue slots, not memory traffic, so a larger U (more accesses in
+// flight, cos/sin reused more) wins over a perfect fit.
+int choose_heads_per_thread(int64_t N, int cap) {
+    for (int u = cap; u > 1; u /= 2) {
+        if (u > N) continue;
+        const int64_t slots = ((N + u - 1) / u) * u;
+        if ((slots - N) * 4 <= slots) return u;
+    }
+    return 1;
+}
+
+rope_status_t make_plan(int dir, int dtype, const void* x, const void* r1, const void* r2,
+                        int64_t N, int64_t D, int64_t start, const Resolved& R, Plan* P) {
+    const int e = R.e;
+    const int64_t a = start * e, Lb = R.L * e, rowb = D * e;
+    const uintptr_t px = reinterpret_cast<uintptr_t>(x), p1 = reinterpret_cast<uintptr_t>(r1),
+                    p2 = reinterpret_cast<uintptr_t>(r2);
+    int vec = 0;
+    for (int v = 16; v >= 4; v /= 2) {
+        if (v < 2 * e) break;  // an access must hold whole pairs
+        bool ok = a % v == 0 && Lb % v == 0 && rowb % v == 0 && px % v == 0 && p1 % v == 0 &&
+                  p2 % v == 0;
+        for (int r = 0; r < 2; ++r)
+            for (int k = 0; k < 3; ++k) ok = ok && R.rb[r][k] % v == 0;
+        if (ok) {
+            vec = v;
+            break;
+        }
+    }
+    P->dtype = dtype;
+    P->dir = dir;
+    if (vec) {
+        P->path = kVector;
+        P->vec = vec;
+        P->C = static_cast<int>(Lb / vec);
+    } else {
+        P->path = kScalarPair;  // odd start, or a row not aligned for wide accesses
+        P->vec = 2 * e;
+        P->C = static_cast<int>(R.L / 2);
+    }
+    P->r_head = R.rb[0][2] != 0 || R.rb[1][2] != 0;
+    P->U = choose_heads_per_thread(N, P->path == kVector && vec == 16 ? 4 : 8);
+    const int64_t H = (N + P->U - 1) / P->U;
+    if (H * P->C > int64_t(kMaxPieceTasks))
+        return fail(ROPE_ERR_INVALID, "N=%lld heads with a %lld-lane slice exceed the per-token work "
+                    "limit of 2^31 accesses", (long long)N, (long long)R.L);
+    P->H = static_cast<int>(H);
+    return ROPE_OK;
+}
+
+KernelArgs base_args(const Plan& P, void* x, const void* r1, const void* r2, int64_t N,
+                     int64_t D, int64_t start, const Resolved& R) {
+    KernelArgs k{};
+    k.x = static_cast<char*>(x) + start * R.e;
+    k.r1 = static_cast<const char*>(r1);
+    k.r2 = static_cast<const char*>(r2);
+    k.row_bytes = D * R.e;
+    k.tok_bytes = N * D * R.e;
+    k.r1_b = R.rb[0][0];
+    k.r1_s = R.rb[0][1];
+    k.r1_n = R.rb[0][2];
+    k.r2_b = R.rb[1][0];
+    k.r2_s = R.rb[1][1];
+    k.r2_n = R.rb[1][2];
+    k.N = static_cast<int32_t>(N);
+    k.H = P.H;
+    k.divC = FastDiv::make(static_cast<uint32_t>(P.C));
+    k.divH = FastDiv::make(static_cast<uint32_t>(P.H));
+    return k;
+}
+
+// A piece: tokens [t0, t0 + count) that are either whole batches (sp == S)
+// or part of one batch (sp == count).
+struct Piece {
+    int64_t b0, s0, count, sp;
+};
+
+template <typename F>
+rope_status_t for_each_piece(int64_t B, int64_t S, int64_t per_tok, F&& f) {
+    const int64_t cap_tokens = int64_t(kMaxPieceTasks) / per_tok;  // >= 1
+    if (B * S <= cap_tokens) return f(Piece{0, 0, B * S, S});
+    if (S <= cap_tokens) {
+        const int64_t nb = cap_tokens / S;
+        for (int64_t b = 0; b < B; b += nb) {
+            const int64_t cnt = (b + nb <= B ? nb : B - b) * S;
+            rope_status_t st = f(Piece{b, 0, cnt, S});
+            if (st != ROPE_OK) return st;
+        }
+        return ROPE_OK;
+    }
+    for (int64_t b = 0; b < B; ++b)
+        for (int64_t s = 0; s < S; s += cap_tokens) {
+            const int64_t cnt = s + cap_tokens <= S ? cap_tokens : S - s;
+            rope_status_t st = f(Piece{b, s, cnt, cnt});
+            if (st != ROPE_OK) return st;
+        }
+    return ROPE_OK;
+}
+
+int64_t grid_for(int64_t tasks, int64_t sms, int64_t blocks_per_sm) {
+    const int64_t need = (tasks + kThreads - 1) / kThreads;
+    const int64_t resident = sms * blocks_per_sm;
+    return need < resident ? need : resident;
+}
+
+rope_status_t run(int dir, void* x, const void* r1, const void* r2, int dtype, int64_t B,
+                  int64_t S, int64_t N, int64_t D, const int64_t* r1_shape,
+                  const int64_t* r1_stride, const int64_t* r2_shape, const int64_t* r2_stride,
+                  int64_t start, int64_t end, rope_stream_t stream) {
+    g_msg[0] = '\0';
+    Resolved R;
+    rope_status_t st = check(x, r1, r2, dtype, B, S, N, D, r1_shape, r1_stride, r2_shape,
+                             r2_stride, start, end, &R);
+    if (st != ROPE_OK || R.empty) return st;
+    Plan P;
+    st = make_plan(dir, dtype, x, r1, r2, N, D, start, R, &P);
+    if (st != ROPE_OK) return st;
+
+    const char* err = nullptr;
+    int sms = 0, bps = 0;
+    if (device_sm_count(&sms, &err) != ROPE_OK) return fail(ROPE_ERR_CUDA, "%s", err);
+    if (kernel_blocks_per_sm(P, &bps, &err) != ROPE_OK) return fail(ROPE_ERR_CUDA, "%s", err);
+    if (bps < 1) bps = 1;
+
+    const KernelArgs whole = base_args(P, x, r1, r2, N, D, start, R);
+    const int64_t per_tok = int64_t(P.H) * P.C;
+    return for_each_piece(B, S, per_tok, [&](const Piece& pc) -> rope_status_t {
+        KernelArgs k = whole;
+        const int64_t t0 = pc.b0 * S + pc.s0;
+        k.x += t0 * whole.tok_bytes;
+        k.r1 += pc.b0 * whole.r1_b + pc.s0 * whole.r1_s;
+        k.r2 += pc.b0 * whole.r2_b + pc.s0 * whole.r2_s;
+        k.tasks = static_cast<uint32_t>(pc.count * per_tok);
+        k.divS = FastDiv::make(static_cast<uint32_t>(pc.sp));
+        const uint32_t blocks = static_cast<uint32_t>(grid_for(k.tasks, sms, bps));
+        const char* e2 = nullptr;
+        if (launch_piece(P, k, blocks, stream, &e2) != ROPE_OK) return fail(ROPE_ERR_CUDA, "%s", e2);
+        return ROPE_OK;
+    });
+}
+
+}  // namespace
+}  // namespace rope
+
+extern "C" {
+
+rope_status_t rope_partial_inplace_fwd(void* x, const void* r1, const void* r2,
+                                       rope_dtype_t dtype, int64_t B, int64_t S, int64_t N,
+                                       int64_t D, const int64_t r1_shape[4],
+                                       const int64_t r1_stride[4], const int64_t r2_shape[4],
+                                       const int64_t r2_stride[4], int64_t start, int64_t end,
+                                       rope_stream_t stream) {
+    return rope::run(rope::kFwd, x, r1, r2, dtype, B, S, N, D, r1_shape, r1_stride, r2_shape,
+                     r2_stride, start, end, stream);
+}
+
+rope_status_t rope_partial_inplace_bwd(void* grad, const void* r1, const void* r2,
+                                       rope_dtype_t dtype, int64_t B, int64_t S, int64_t N,
+                                       int64_t D, const int64_t r1_shape[4],
+                                       const int64_t r1_stride[4], const int64_t r2_shape[4],
+                                       const int64_t r2_stride[4], int64_t start, int64_t end,
+                                       rope_stream_t stream) {
+    return rope::run(rope::kBwd, grad, r1, r2, dtype, B, S, N, D, r1_shape, r1_stride, r2_shape,
+                     r2_stride, start, end, stream);
+}
+
+const char* rope_status_str(rope_status_t status) {
+    switch (status) {
+        case ROPE_OK: return "ROPE_OK";
+        case ROPE_ERR_NULLPTR: return "ROPE_ERR_NULLPTR";
+        case ROPE_ERR_INVALID: return "ROPE_ERR_INVALID";
+        case ROPE_ERR_CUDA: return "ROPE_ERR_CUDA";
+    }
+    return "ROPE_ERR_UNKNOWN";
+}
+
+const char* rope_last_error_message(void) { return rope::g_msg; }
+
+rope_status_t rope_partial_plan(const void* x, const void* r1, const void* r2,
+                                rope_dtype_t dtype, int64_t B, int64_t S, int64_t N, int64_t D,
+                                const int64_t r1_shape[4], const int64_t r1_stride[4],
+                                const int64_t r2_shape[4], const int64_t r2_stride[4],
+                                int64_t start, int64_t end, int32_t sm_count,
+                                rope_plan_t* plan) {
+    using namespace rope;
+    g_msg[0] = '\0';
+    if (!plan) return fail(ROPE_ERR_NULLPTR, "plan is null");
+    *plan = rope_plan_t{};
+    Resolved R;
+    rope_status_t st = check(x, r1, r2, dtype, B, S, N, D, r1_shape, r1_stride, r2_shape,
+                             r2_stride, start, end, &R);
+    if (st != ROPE_OK || R.empty) return st;
+    Plan P;
+    st = make_plan(kFwd, dtype, x, r1, r2, N, D, start, R, &P);
+    if (st != ROPE_OK) return st;
+    int sms = sm_count, bps = kBlocksPerSmCap;
+    if (sm_count <= 0) {
+        const char* err = nullptr;
+        if (device_sm_count(&sms, &err) != ROPE_OK) return fail(ROPE_ERR_CUDA, "%s", err);
+        if (kernel_blocks_per_sm(P, &bps, &err) != ROPE_OK) return fail(ROPE_ERR_CUDA, "%s", err);
+    }
+    const int64_t per_tok = int64_t(P.H) * P.C;
+    int64_t max_blocks = 0, launches = 0;
+    for_each_piece(B, S, per_tok, [&](const Piece& pc) -> rope_status_t {
+        const int64_t g = grid_for(pc.count * per_tok, sms, bps);
+        if (g > max_blocks) max_blocks = g;
+        ++launches;
+        return ROPE_OK;
+    });
+    plan->path = P.path;
+    plan->vec_bytes = P.vec;
+    plan->heads_per_thread = P.U;
+    plan->threads_per_block = kThreads;
+    plan->blocks = max_blocks;
+    plan->tasks = B * S * per_tok;
+    plan->chunks_per_row = P.C;
+    plan->r_per_head = P.r_head ? 1 : 0;
+    plan->launches = launches;
+    return ROPE_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,58 @@
+// rope_internal.h -- what the host planner hands to the launcher.
+// Not part of the public ABI (that is include/rope_partial.h).
+#pragma once
+#include <stdint.h>
+
+#include "fast_div.h"
+#include "rope_partial.h"
+
+namespace rope {
+
+constexpr int kThreads = 256;            // threads per block
+constexpr int kBlocksPerSmCap = 8;       // 2048 resident threads per SM / 256
+constexpr uint32_t kMaxPieceTasks = 1u << 31;  // flat work index of one launch
+
+enum Direction : int { kFwd = 0, kBwd = 1 };
+enum Path : int { kNone = 0, kVector = 1, kScalarPair = 2 };
+
+// What one launch covers: a contiguous range of tokens ("a piece").  The
+// kernel turns its flat work index into (token, head group, chunk) with
+// three fast divisions, then into byte offsets from the piece's bases.
+struct KernelArgs {
+    char* x;                   // row 0 of the piece's first token, plus start * e
+    const char* r1;            // cos of the piece's first (batch, seq) position
+    const char* r2;            // sin of the same
+    int64_t tok_bytes;         // bytes between consecutive tokens of x (N * D * e)
+    int64_t row_bytes;         // bytes between consecutive heads of x (D * e)
+    int64_t r1_b, r1_s, r1_n;  // byte strides of r1 for batch, seq, head (0: broadcast)
+    int64_t r2_b, r2_s, r2_n;
+    uint32_t tasks;            // work items of the piece: tokens * H * C
+    int32_t N;                 // heads
+    int32_t H;                 // head groups = ceil(N / U)
+    FastDiv divC;              // chunks per row
+    FastDiv divH;              // head groups
+    FastDiv divS;              // tokens per batch inside the piece
+};
+
+// The kernel a validated call runs.
+struct Plan {
+    int dtype;      // rope_dtype_t
+    int dir;        // Direction
+    int path;       // Path
+    int vec;        // bytes per access of x: 16, 8 or 4 (vector), 2 * e (scalar pair)
+    int U;          // heads per thread (cos/sin reused from registers across them)
+    int H;          // head groups
+    int C;          // chunks (accesses) per row slice
+    bool r_head;    // cos/sin differ between heads: reloaded per head
+};
+
+// Launch one piece on `stream` with `blocks` blocks (defined in the .cu).
+rope_status_t launch_piece(const Plan& plan, const KernelArgs& args, uint32_t blocks,
+                           rope_stream_t stream, const char** err);
+
+// The current device's SM count and the planned kernel's resident blocks
+// per SM (defined in the .cu; the only device queries the library makes).
+rope_status_t device_sm_count(int* sms, const char** err);
+rope_status_t kernel_blocks_per_sm(const Plan& plan, int* blocks, const char** err);
+
+}  // namespace rope

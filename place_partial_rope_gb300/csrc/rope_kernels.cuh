@@ -1,0 +1,326 @@
+// rope_kernels.cuh -- the sm_103a kernel of the in-place partial interleaved
+// rotary embedding, forward and backward, for bf16 / fp16 / fp32 storage.
+//
+// What it computes ("CANN ops-transformer inplace_partial_rotary_mul",
+// section 功能与计算公式, and its kernel op chain): for every row
+// (b, s, n) of a BSND tensor and every pair (2i, 2i+1) of the slice
+// [start, end) counted from start,
+//   forward : y0 = x0*c0 - x1*s0          y1 = x1*c1 + x0*s1
+//   backward: d0 = g0*c0 + g1*s1          d1 = g1*c1 - g0*s0
+// Inputs are widened to fp32, each product and each sum is one fp32 rounding
+// (__fmul_rn / __fadd_rn / __fsub_rn, which the compiler never contracts
+// into an FMA), and the result is rounded once to the storage type with
+// round-to-nearest-even (the page's CAST_RINT write-back).
+//
+// How (GB300): the op is a streaming read-modify-write of the slice bytes,
+// bound by HBM bandwidth, so there is no tensor-core work and no shared
+// memory.  One work item is (token, head group, chunk):
+//   * a chunk is one 16-, 8- or 4-byte access of x that holds whole pairs,
+//     so the pair swap happens inside a thread's registers (no shuffles);
+//     rows whose slice is not aligned for that fall back to a scalar path
+//     with one access per element ("scalar pair");
+//   * a thread keeps the chunk's cos/sin in registers and walks U heads of
+//     the same token (heads hg, hg+H, ..., H = ceil(N/U)), issuing all U
+//     loads of x before any arithmetic, so U accesses per thread are in
+//     flight and the cos/sin bytes are read once per U heads;
+//   * consecutive threads take consecutive chunks of a row, so a warp reads
+//     whole 32-byte sectors of each row's slice;
+//   * the grid is sized to the resident blocks of all SMs and strides over
+//     the flat work index (three multiply-high divisions per item).
+// Only slice bytes are read or written; every other byte of x is untouched.
+#pragma once
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "rope_internal.h"
+
+namespace rope {
+
+template <int W>
+struct Words {
+    uint32_t w[W];
+};
+
+// ------------------------------------------------------------------------
+// storage packing: pairs <-> 32-bit words
+// ------------------------------------------------------------------------
+
+template <typename T>
+struct Pack;
+
+template <>
+struct Pack<float> {
+    static constexpr int kWordsPerPair = 2;
+    static __device__ __forceinline__ void get(const uint32_t* w, float& a, float& b) {
+        a = __uint_as_float(w[0]);
+        b = __uint_as_float(w[1]);
+    }
+    static __device__ __forceinline__ void put(uint32_t* w, float a, float b) {
+        w[0] = __float_as_uint(a);
+        w[1] = __float_as_uint(b);
+    }
+};
+
+template <>
+struct Pack<__nv_bfloat16> {
+    static constexpr int kWordsPerPair = 1;
+    // a bfloat16 is the top half of a binary32: widening is a shift
+    static __device__ __forceinline__ void get(const uint32_t* w, float& a, float& b) {
+        a = __uint_as_float(w[0] << 16);
+        b = __uint_as_float(w[0] & 0xffff0000u);
+    }
+    static __device__ __forceinline__ void put(uint32_t* w, float a, float b) {
+        const __nv_bfloat162 h = __floats2bfloat162_rn(a, b);  // .x (low half) = a
+        uint32_t u;
+        memcpy(&u, &h, 4);
+        w[0] = u;
+    }
+};
+
+template <>
+struct Pack<__half> {
+    static constexpr int kWordsPerPair = 1;
+    static __device__ __forceinline__ void get(const uint32_t* w, float& a, float& b) {
+        __half2 h;
+        memcpy(&h, &w[0], 4);
+        const float2 f = __half22float2(h);
+        a = f.x;
+        b = f.y;
+    }
+    static __device__ __forceinline__ void put(uint32_t* w, float a, float b) {
+        const __half2 h = __floats2half2_rn(a, b);  // .x (low half) = a
+        uint32_t u;
+        memcpy(&u, &h, 4);
+        w[0] = u;
+    }
+};
+
+// ------------------------------------------------------------------------
+// global memory: x (read then written by the same thread) and cos/sin
+// (read-only for the whole kernel, so they may take the non-coherent path)
+// ------------------------------------------------------------------------
+
+template <int W>
+__device__ __forceinline__ Words<W> ld_vec(const char* p) {
+    Words<W> v;
+    if constexpr (W == 4) {
+        const uint4 q = *reinterpret_cast<const uint4*>(p);
+        v.w[0] = q.x; v.w[1] = q.y; v.w[2] = q.z; v.w[3] = q.w;
+    } else if constexpr (W == 2) {
+        const uint2 q = *reinterpret_cast<const uint2*>(p);
+        v.w[0] = q.x; v.w[1] = q.y;
+    } else {
+        v.w[0] = *reinterpret_cast<const uint32_t*>(p);
+    }
+    return v;
+}
+
+template <int W>
+__device__ __forceinline__ Words<W> ldg_vec(const char* p) {
+    Words<W> v;
+    if constexpr (W == 4) {
+        const uint4 q = __ldg(reinterpret_cast<const uint4*>(p));
+        v.w[0] = q.x; v.w[1] = q.y; v.w[2] = q.z; v.w[3] = q.w;
+    } else if constexpr (W == 2) {
+        const uint2 q = __ldg(reinterpret_cast<const uint2*>(p));
+        v.w[0] = q.x; v.w[1] = q.y;
+    } else {
+        v.w[0] = __ldg(reinterpret_cast<const unsigned int*>(p));
+    }
+    return v;
+}
+
+template <int W>
+__device__ __forceinline__ void st_vec(char* p, const Words<W>& v) {
+    if constexpr (W == 4) {
+        *reinterpret_cast<uint4*>(p) = make_uint4(v.w[0], v.w[1], v.w[2], v.w[3]);
+    } else if constexpr (W == 2) {
+        *reinterpret_cast<uint2*>(p) = make_uint2(v.w[0], v.w[1]);
+    } else {
+        *reinterpret_cast<uint32_t*>(p) = v.w[0];
+    }
+}
+
+// One pair through element-sized accesses (any element-aligned address).
+template <typename T, bool RO>
+__device__ __forceinline__ Words<Pack<T>::kWordsPerPair> ld_pair_scalar(const char* p) {
+    Words<Pack<T>::kWordsPerPair> v;
+    if constexpr (sizeof(T) == 4) {
+        const unsigned int* q = reinterpret_cast<const unsigned int*>(p);
+        v.w[0] = RO ? __ldg(q) : q[0];
+        v.w[1] = RO ? __ldg(q + 1) : q[1];
+    } else {
+        const unsigned short* q = reinterpret_cast<const unsigned short*>(p);
+        const uint32_t lo = RO ? __ldg(q) : q[0];
+        const uint32_t hi = RO ? __ldg(q + 1) : q[1];
+        v.w[0] = lo | (hi << 16);
+    }
+    return v;
+}
+
+template <typename T>
+__device__ __forceinline__ void st_pair_scalar(char* p, const Words<Pack<T>::kWordsPerPair>& v) {
+    if constexpr (sizeof(T) == 4) {
+        unsigned int* q = reinterpret_cast<unsigned int*>(p);
+        q[0] = v.w[0];
+        q[1] = v.w[1];
+    } else {
+        unsigned short* q = reinterpret_cast<unsigned short*>(p);
+        q[0] = static_cast<unsigned short>(v.w[0] & 0xffffu);
+        q[1] = static_cast<unsigned short>(v.w[0] >> 16);
+    }
+}
+
+template <typename T, int W, bool SCALAR>
+__device__ __forceinline__ Words<W> load_x(const char* p) {
+    if constexpr (SCALAR) return ld_pair_scalar<T, false>(p);
+    else return ld_vec<W>(p);
+}
+
+template <typename T, int W, bool SCALAR>
+__device__ __forceinline__ Words<W> load_r(const char* p) {
+    if constexpr (SCALAR) return ld_pair_scalar<T, true>(p);
+    else return ldg_vec<W>(p);
+}
+
+template <typename T, int W, bool SCALAR>
+__device__ __forceinline__ void store_x(char* p, const Words<W>& v) {
+    if constexpr (SCALAR) st_pair_scalar<T>(p, v);
+    else st_vec<W>(p, v);
+}
+
+// ------------------------------------------------------------------------
+// the rotation of one pair, in the page's rounding order
+// ------------------------------------------------------------------------
+
+template <int DIR>
+__device__ __forceinline__ void rotate_pair(float x0, float x1, float c0, float c1, float s0,
+                                            float s1, float& y0, float& y1) {
+    if constexpr (DIR == kFwd) {
+        y0 = __fsub_rn(__fmul_rn(x0, c0), __fmul_rn(x1, s0));
+        y1 = __fadd_rn(__fmul_rn(x1, c1), __fmul_rn(x0, s1));
+    } else {
+        y0 = __fadd_rn(__fmul_rn(x0, c0), __fmul_rn(x1, s1));
+        y1 = __fsub_rn(__fmul_rn(x1, c1), __fmul_rn(x0, s0));
+    }
+}
+
+template <typename T, int W, int DIR>
+__device__ __forceinline__ Words<W> rotate_chunk(const Words<W>& x, const Words<W>& c,
+                                                 const Words<W>& s) {
+    using P = Pack<T>;
+    constexpr int WPP = P::kWordsPerPair;
+    Words<W> y;
+#pragma unroll
+    for (int p = 0; p < W / WPP; ++p) {
+        float x0, x1, c0, c1, s0, s1, y0, y1;
+        P::get(&x.w[p * WPP], x0, x1);
+        P::get(&c.w[p * WPP], c0, c1);
+        P::get(&s.w[p * WPP], s0, s1);
+        rotate_pair<DIR>(x0, x1, c0, c1, s0, s1, y0, y1);
+        P::put(&y.w[p * WPP], y0, y1);
+    }
+    return y;
+}
+
+// ------------------------------------------------------------------------
+// the kernel
+//   T      storage type            VEC    bytes per access of x
+//   SCALAR element-wise accesses   U      heads per thread
+//   DIR    kFwd / kBwd             RHEAD  cos/sin differ between heads
+// ------------------------------------------------------------------------
+
+template <typename T, int VEC, bool SCALAR, int U, int DIR, bool RHEAD>
+__global__ void __launch_bounds__(kThreads) rope_partial_kernel(const KernelArgs a) {
+    constexpr int W = VEC / 4;
+    char* const __restrict__ xbase = a.x;
+    const char* const __restrict__ r1base = a.r1;
+    const char* const __restrict__ r2base = a.r2;
+    const int64_t xstep = int64_t(a.H) * a.row_bytes;  // to the next head of this thread
+    const uint64_t stride = uint64_t(gridDim.x) * kThreads;
+
+    for (uint64_t t = uint64_t(blockIdx.x) * kThreads + threadIdx.x; t < a.tasks; t += stride) {
+        uint32_t rest, c, tok, hg, b, s;
+        a.divC.divmod(uint32_t(t), rest, c);
+        a.divH.divmod(rest, tok, hg);
+        a.divS.divmod(tok, b, s);
+
+        char* xp = xbase + int64_t(tok) * a.tok_bytes + int64_t(hg) * a.row_bytes +
+                   int64_t(c) * VEC;
+        const char* c_p = r1base + int64_t(b) * a.r1_b + int64_t(s) * a.r1_s + int64_t(c) * VEC;
+        const char* s_p = r2base + int64_t(b) * a.r2_b + int64_t(s) * a.r2_s + int64_t(c) * VEC;
+        if constexpr (RHEAD) {
+            c_p += int64_t(hg) * a.r1_n;
+            s_p += int64_t(hg) * a.r2_n;
+        }
+
+        Words<W> xv[U];
+#pragma unroll
+        for (int i = 0; i < U; ++i)
+            if (i == 0 || int(hg) + i * a.H < a.N) xv[i] = load_x<T, W, SCALAR>(xp + i * xstep);
+
+        Words<W> cv, sv;
+        if constexpr (!RHEAD) {
+            cv = load_r<T, W, SCALAR>(c_p);
+            sv = load_r<T, W, SCALAR>(s_p);
+        }
+#pragma unroll
+        for (int i = 0; i < U; ++i) {
+            if (i == 0 || int(hg) + i * a.H < a.N) {
+                if constexpr (RHEAD) {
+                    cv = load_r<T, W, SCALAR>(c_p + int64_t(i) * a.H * a.r1_n);
+                    sv = load_r<T, W, SCALAR>(s_p + int64_t(i) * a.H * a.r2_n);
+                }
+                store_x<T, W, SCALAR>(xp + i * xstep, rotate_chunk<T, W, DIR>(xv[i], cv, sv));
+            }
+        }
+    }
+}
+
+// ------------------------------------------------------------------------
+// kernel selection for one storage type (instantiated in one .cu per type)
+// ------------------------------------------------------------------------
+
+template <typename T, int VEC, bool SCALAR, int U>
+const void* pick_dir(const Plan& p) {
+    if (p.dir == kFwd)
+        return p.r_head ? reinterpret_cast<const void*>(&rope_partial_kernel<T, VEC, SCALAR, U, kFwd, true>)
+                        : reinterpret_cast<const void*>(&rope_partial_kernel<T, VEC, SCALAR, U, kFwd, false>);
+    return p.r_head ? reinterpret_cast<const void*>(&rope_partial_kernel<T, VEC, SCALAR, U, kBwd, true>)
+                    : reinterpret_cast<const void*>(&rope_partial_kernel<T, VEC, SCALAR, U, kBwd, false>);
+}
+
+template <typename T, int VEC, bool SCALAR>
+const void* pick_heads(const Plan& p) {
+    switch (p.U) {
+        case 1: return pick_dir<T, VEC, SCALAR, 1>(p);
+        case 2: return pick_dir<T, VEC, SCALAR, 2>(p);
+        case 4: return pick_dir<T, VEC, SCALAR, 4>(p);
+        case 8:
+            if constexpr (VEC < 16) return pick_dir<T, VEC, SCALAR, 8>(p);
+            else return nullptr;
+        default: return nullptr;
+    }
+}
+
+template <typename T>
+const void* pick_kernel(const Plan& p) {
+    if (p.path == kScalarPair) return pick_heads<T, 2 * sizeof(T), true>(p);
+    switch (p.vec) {
+        case 16: return pick_heads<T, 16, false>(p);
+        case 8: return pick_heads<T, 8, false>(p);
+        case 4:
+            if constexpr (sizeof(T) == 2) return pick_heads<T, 4, false>(p);
+            else return nullptr;
+        default: return nullptr;
+    }
+}
+
+// defined in rope_kernels_{bf16,fp16,fp32}.cu
+const void* kernel_for_bf16(const Plan& p);
+const void* kernel_for_fp16(const Plan& p);
+const void* kernel_for_fp32(const Plan& p);
+
+}  // namespace rope

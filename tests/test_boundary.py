@@ -1,0 +1,229 @@
+"""The C ABI without a GPU: exports, validation, empty calls and launch plans.
+
+Every call here is rejected or empty (returns before any CUDA call), or is a
+plan query with an explicit SM count, so nothing touches a device.  Fake
+pointers are plain aligned integers and are never dereferenced.
+
+The rules follow "CANN ops-transformer inplace_partial_rotary_mul", section
+约束说明 (D even and <= 1024; 0 <= start <= end <= D with an even length;
+r1/r2 broadcast against the slice with last dim end - start; one dtype),
+and section 功能与计算公式 (start == end is a no-op; the backward accepts
+empty tensors).
+"""
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+from place_partial_rope_gb300 import binding, build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "rope_partial.h")
+OK, NULLPTR, INVALID, CUDA = 0, 1, 2, 3
+BF16, FP16, FP32 = 0, 1, 2
+BASE = 0x7F0000000000  # a fake, 256-byte aligned device address
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build.build()
+    return binding.load_library()
+
+
+def i64(*v):
+    return (ctypes.c_int64 * 4)(*v)
+
+
+def contig(shape):
+    B, S, N, L = shape
+    return (S * N * L, N * L, L, 1)
+
+
+def call(lib, fn="rope_partial_inplace_fwd", x=BASE, r1=BASE + 2**30, r2=BASE + 2**31,
+         dtype=FP16, shape=(2, 4, 3, 16), start=0, end=8, r_shape=None, r_stride=None,
+         r2_shape=None, r2_stride=None):
+    B, S, N, D = shape
+    rs = r_shape if r_shape is not None else (1, S, 1, end - start)
+    rst = r_stride if r_stride is not None else (contig(rs) if rs != "null" else (0, 0, 0, 1))
+    r2s = r2_shape if r2_shape is not None else rs
+    r2st = r2_stride if r2_stride is not None else (contig(r2s) if r2s != "null" else (0, 0, 0, 1))
+    a1 = i64(*rs) if rs != "null" else None
+    a2 = i64(*rst) if rst != "null" else None
+    a3 = i64(*r2s) if r2s != "null" else None
+    a4 = i64(*r2st) if r2st != "null" else None
+    return getattr(lib, fn)(x, r1, r2, dtype, B, S, N, D, a1, a2, a3, a4, start, end, None)
+
+
+def test_header_symbols_are_exported(lib):
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    names = set(re.findall(r"\b(rope_[a-z_]+)\s*\(", text))
+    assert names == {"rope_partial_inplace_fwd", "rope_partial_inplace_bwd", "rope_status_str",
+                     "rope_last_error_message", "rope_partial_plan"}
+    for n in names:
+        assert hasattr(lib, n), n
+    nm = subprocess.run(["nm", "-D", "--defined-only", binding.library_path()],
+                        capture_output=True, text=True, check=True).stdout
+    exported = set(re.findall(r"\bT (rope_\w+)", nm))
+    assert names <= exported
+
+
+def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
+    monkeypatch.setattr(binding, "_LIB_PATH", str(tmp_path / "missing.so"))
+    monkeypatch.setattr(binding, "_lib", None)
+    with pytest.raises(RuntimeError, match="no CPU fallback"):
+        binding.load_library()
+
+
+def test_status_strings(lib):
+    assert lib.rope_status_str(OK) == b"ROPE_OK"
+    assert lib.rope_status_str(INVALID) == b"ROPE_ERR_INVALID"
+    assert lib.rope_status_str(CUDA) == b"ROPE_ERR_CUDA"
+    assert lib.rope_status_str(99) == b"ROPE_ERR_UNKNOWN"
+
+
+@pytest.mark.parametrize("fn", ["rope_partial_inplace_fwd", "rope_partial_inplace_bwd"])
+@pytest.mark.parametrize("kwargs,status,needle", [
+    (dict(dtype=3), INVALID, "dtype"),
+    (dict(dtype=-1), INVALID, "dtype"),
+    (dict(shape=(-1, 4, 3, 16)), INVALID, "negative"),
+    (dict(shape=(2, 4, 3, 15), end=8), INVALID, "even"),
+    (dict(shape=(1, 1, 1, 1026), end=2), INVALID, "1024"),
+    (dict(start=-2, end=4), INVALID, "slice"),
+    (dict(start=10, end=8), INVALID, "slice"),
+    (dict(start=0, end=18), INVALID, "slice"),
+    (dict(start=1, end=8), INVALID, "even"),
+    (dict(r_shape=(1, 3, 1, 8)), INVALID, "broadcast"),
+    (dict(r_shape=(2, 4, 2, 8)), INVALID, "broadcast"),
+    (dict(r_shape=(1, 4, 1, 6)), INVALID, "last dim"),
+    (dict(r2_shape=(1, 4, 1, 4)), INVALID, "r2 last dim"),
+    (dict(r_stride=(32, 8, 8, 2)), INVALID, "contiguous"),
+    (dict(r_stride=(32, -8, 8, 1)), INVALID, "negative"),
+    (dict(x=0), NULLPTR, "x is null"),
+    (dict(r1=0), NULLPTR, "r1"),
+    (dict(r2=0), NULLPTR, "r2"),
+    (dict(r_shape="null"), NULLPTR, "r1_shape"),
+    (dict(r2_stride="null"), NULLPTR, "r2_stride"),
+    (dict(x=BASE + 1), INVALID, "aligned"),
+    (dict(dtype=FP32, x=BASE + 2), INVALID, "aligned"),
+    (dict(r1=BASE + 3), INVALID, "aligned"),
+])
+def test_rejected_calls(lib, fn, kwargs, status, needle):
+    st = call(lib, fn, **kwargs)
+    assert st == status, (st, lib.rope_last_error_message())
+    assert needle in lib.rope_last_error_message().decode()
+
+
+@pytest.mark.parametrize("fn", ["rope_partial_inplace_fwd", "rope_partial_inplace_bwd"])
+@pytest.mark.parametrize("kwargs", [
+    dict(start=4, end=4, x=0, r1=0, r2=0),                      # empty slice, null pointers
+    dict(start=0, end=0, x=0, r1=0, r2=0, r_shape="null", r2_shape="null",
+         r_stride="null", r2_stride="null"),                    # nothing at all
+    dict(shape=(0, 4, 3, 16), x=0, r1=0, r2=0, r_shape=(1, 4, 1, 8)),   # B == 0
+    dict(shape=(2, 0, 3, 16), r_shape=(1, 0, 1, 8)),            # S == 0
+    dict(shape=(2, 4, 0, 16), r_shape=(1, 4, 1, 8)),            # N == 0
+    dict(shape=(2, 4, 3, 0), start=0, end=0, r_shape=(1, 4, 1, 0)),  # D == 0
+])
+def test_empty_calls_are_noops(lib, fn, kwargs):
+    assert call(lib, fn, **kwargs) == OK, lib.rope_last_error_message()
+
+
+def plan(lib, x=BASE, r1=BASE + 2**30, r2=BASE + 2**31, dtype=FP16, shape=(2, 4, 3, 16),
+         start=0, end=8, r_shape=None, r_stride=None, sms=152):
+    B, S, N, D = shape
+    rs = r_shape or (1, S, 1, end - start)
+    rst = r_stride or contig(rs)
+    p = binding.RopePlan()
+    st = lib.rope_partial_plan(x, r1, r2, dtype, B, S, N, D, i64(*rs), i64(*rst), i64(*rs),
+                               i64(*rst), start, end, sms, ctypes.byref(p))
+    assert st == OK, lib.rope_last_error_message()
+    return p
+
+
+def test_plans_of_the_named_workloads(lib):
+    # GQA fp16: 128-byte slices at offset 0 of 256-byte rows -> 16-byte accesses
+    p = plan(lib, dtype=FP16, shape=(32, 2048, 16, 128), start=0, end=64, r_shape=(1, 2048, 1, 64))
+    assert (p.path, p.vec_bytes, p.chunks_per_row, p.heads_per_thread, p.r_per_head) == (1, 16, 8, 4, 0)
+    assert p.tasks == 32 * 2048 * 4 * 8 and p.blocks == 152 * 8 and p.launches == 1
+    # MLA-decode query bf16: one cos/sin row per token
+    p = plan(lib, dtype=BF16, shape=(4096, 1, 128, 192), start=0, end=64, r_shape=(4096, 1, 1, 64))
+    assert (p.path, p.vec_bytes, p.chunks_per_row, p.heads_per_thread) == (1, 16, 8, 4)
+    # large fp32 with the slice at byte 136: 8-byte accesses hold whole pairs
+    p = plan(lib, dtype=FP32, shape=(4, 8192, 32, 128), start=34, end=98, r_shape=(4, 8192, 1, 64))
+    assert (p.path, p.vec_bytes, p.chunks_per_row, p.heads_per_thread) == (1, 8, 32, 8)
+    # tiny fp32 and the small-model bf16 full-row slice
+    p = plan(lib, dtype=FP32, shape=(1, 16, 2, 64), start=0, end=32, r_shape=(1, 16, 1, 32))
+    assert (p.path, p.vec_bytes, p.heads_per_thread, p.blocks) == (1, 16, 2, 1)
+    p = plan(lib, dtype=BF16, shape=(16, 256, 12, 64), start=0, end=64, r_shape=(1, 256, 1, 64))
+    assert (p.path, p.vec_bytes, p.heads_per_thread) == (1, 16, 4)
+
+
+def test_path_choice(lib):
+    assert plan(lib, start=1, end=9).path == 2                       # odd start: scalar pairs
+    assert plan(lib, dtype=FP32, start=1, end=9).path == 2
+    assert plan(lib, start=2, end=10).vec_bytes == 4                 # 4-byte slice offset
+    assert plan(lib, x=BASE + 8).vec_bytes == 8                      # x only 8-byte aligned
+    assert plan(lib, r1=BASE + 2**30 + 4).vec_bytes == 4             # cos only 4-byte aligned
+    assert plan(lib, dtype=FP32, x=BASE + 4).path == 2               # fp32 pairs need 8 bytes
+    assert plan(lib, shape=(2, 4, 3, 18), end=8).vec_bytes == 4      # 36-byte rows
+    p = plan(lib, r_shape=(2, 4, 3, 8))                               # cos/sin per head (BSND)
+    assert p.r_per_head == 1
+    assert plan(lib, r_shape=(1, 4, 3, 8)).r_per_head == 1           # 1SND
+    assert plan(lib, r_shape=(2, 1, 1, 8)).r_per_head == 0           # B11D
+
+
+@pytest.mark.parametrize("N,vec,U", [(1, 16, 1), (2, 16, 2), (3, 16, 2), (5, 16, 2), (7, 16, 4),
+                                     (12, 16, 4), (16, 16, 4), (12, 8, 8), (32, 8, 8), (6, 8, 4)])
+def test_heads_per_thread(lib, N, vec, U):
+    start = 0 if vec == 16 else 4  # 8-byte slice offset forces 8-byte accesses for fp16
+    p = plan(lib, shape=(1, 2, N, 24), start=start, end=start + 8, r_shape=(1, 2, 1, 8))
+    assert p.vec_bytes == vec and p.heads_per_thread == U
+
+
+def test_huge_calls_split_into_launches(lib):
+    # fp16 rows of 2 elements, one head: one work item per token
+    p = plan(lib, shape=(2, 2**30 + 3, 1, 2), start=0, end=2, r_shape=(1, 2**30 + 3, 1, 2))
+    assert p.launches == 2 and p.tasks == 2 * (2**30 + 3)            # whole batches per launch
+    p = plan(lib, shape=(1, 2**31 + 5, 1, 2), start=0, end=2, r_shape=(1, 2**31 + 5, 1, 2))
+    assert p.launches == 2                                           # runs of tokens of one batch
+    p = plan(lib, shape=(3, 2**31 + 5, 1, 2), start=0, end=2, r_shape=(1, 2**31 + 5, 1, 2))
+    assert p.launches == 6
+    p = plan(lib, shape=(2**20, 2**11, 1, 2), start=0, end=2, r_shape=(1, 2**11, 1, 2))
+    assert p.launches == 1                                           # exactly 2^31 items
+
+
+def test_fast_division_exhaustive_sample(tmp_path):
+    """The multiply-high division used by the kernels, against / and %."""
+    src = tmp_path / "t.cpp"
+    src.write_text(r'''
+#include "fast_div.h"
+#include <cstdio>
+#include <cstdint>
+int main() {
+  uint64_t bad = 0, n_checked = 0;
+  uint32_t divs[] = {1u,2u,3u,5u,7u,8u,12u,31u,32u,64u,96u,128u,255u,1000u,2048u,4095u,65537u,
+                     (1u<<20)+7u,(1u<<30)+3u,(1u<<31)-1u,(1u<<31),(1u<<31)+1u,4294967295u};
+  for (uint32_t d : divs) {
+    rope::FastDiv f = rope::FastDiv::make(d);
+    for (uint64_t n = 0; n < (1ull<<32); n += 0x10001ull + d) {
+      uint32_t q, r; f.divmod((uint32_t)n, q, r); ++n_checked;
+      if (q != (uint32_t)n / d || r != (uint32_t)n % d) ++bad;
+    }
+    for (uint64_t k = 0; k < 4096; ++k) {
+      uint32_t n = 0xffffffffu - (uint32_t)k, q, r; f.divmod(n, q, r); ++n_checked;
+      if (q != n / d || r != n % d) ++bad;
+      n = (uint32_t)k * d; f.divmod(n, q, r); if (q != n / d || r != n % d) ++bad;
+      if (n) { --n; f.divmod(n, q, r); if (q != n / d || r != n % d) ++bad; }
+    }
+  }
+  std::printf("%llu %llu\n", (unsigned long long)bad, (unsigned long long)n_checked);
+  return bad != 0;
+}
+''')
+    exe = tmp_path / "t"
+    subprocess.run(["g++", "-O2", "-std=c++17", "-I", os.path.join(build.CSRC), str(src), "-o",
+                    str(exe)], check=True)
+    out = subprocess.run([str(exe)], capture_output=True, text=True)
+    assert out.returncode == 0, out.stdout
