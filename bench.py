@@ -1,0 +1,548 @@
+#!/usr/bin/env python
+"""Throughput of the in-place partial interleaved rotary embedding on GB300.
+
+One step = the forward on x followed by the backward on a gradient of the
+same shape (two launches), over the largest configuration: fp32 x of shape
+(4, 8192, 32, 128) whose slice [34, 98) is rotated, with one cos/sin row per
+(batch, position) of shape (4, 8192, 1, 64).  Inputs are seeded synthetic
+data (N(0, 1) activations and gradients, a base-10000 cos/sin table over
+per-batch position offsets) resident in HBM before timing; x and grad
+(537 MB each) exceed the 129 MB L2, so no flush is needed between steps.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+
+Prints ONE JSON line on rank 0.  `value` is the algorithmic bytes of all
+ranks (slice bytes read + written plus the unique cos/sin bytes, per launch)
+divided by the slowest rank's device time.  Under torchrun each rank runs
+its own copy of the workload on its own GPU (weak scaling; no collective on
+the data path, only a max-reduction of the timings).
+
+`--impl reference` times the CPU oracle on the host cores instead, on a
+bounded sample of the same workload, with the same metric.
+"""
+from __future__ import annotations
+
+import argparse
+import ctypes
+import hashlib
+import json
+import os
+import re
+import statistics
+import subprocess
+import sys
+import threading
+import time
+from concurrent.futures import ThreadPoolExecutor
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+from place_partial_rope_gb300 import synth  # noqa: E402
+
+METRIC = "in-place partial RoPE fwd/bwd achieved HBM GB/s and % of GB300 peak"
+HEADLINE = "large_unaligned"
+FALLBACK_HBM_GBS = 6800.0
+CSRC = os.path.join(ROOT, "place_partial_rope_gb300", "csrc")
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "ncu_traffic.md")
+
+
+# --------------------------------------------------------------------------
+# small utilities
+# --------------------------------------------------------------------------
+
+def kernel_source_hash() -> str:
+    """Hash of the kernel sources, to tell whether stored ncu counters still
+    describe the kernel that runs."""
+    h = hashlib.sha256()
+    for f in sorted(os.listdir(CSRC)):
+        if f.endswith((".cu", ".cuh", ".h", ".cpp")):
+            with open(os.path.join(CSRC, f), "rb") as fh:
+                h.update(f.encode() + b"\0" + fh.read())
+    return h.hexdigest()[:16]
+
+
+def stored_traffic(kernel: str, workload: str):
+    """DRAM bytes per launch from the committed ncu summary, or None when the
+    summary is missing or was taken on other kernel sources."""
+    if not os.path.exists(TRAFFIC_FILE):
+        return None
+    pat = re.compile(r"traffic:\s*kernel=(\S+)\s+workload=(\S+)\s+source_sha=(\S+)\s+"
+                     r"dram_bytes_per_launch=(\d+)")
+    src = kernel_source_hash()
+    with open(TRAFFIC_FILE) as f:
+        for line in f:
+            m = pat.search(line)
+            if m and m.group(1) == kernel and m.group(2) == workload and m.group(3) == src:
+                return int(m.group(4))
+    return None
+
+
+def kernel_name(plan, dtype: str, direction: int) -> str:
+    """The template instance a plan runs, as ncu names it (without spaces)."""
+    ctype = {"fp32": "float", "bf16": "__nv_bfloat16", "fp16": "__half"}[dtype]
+    scalar = "true" if plan.path == 2 else "false"
+    rhead = "true" if plan.r_per_head else "false"
+    return (f"rope_partial_kernel<{ctype},{plan.vec_bytes},{scalar},{plan.heads_per_thread},"
+            f"{direction},{rhead}>")
+
+
+def hbm_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def host_cores() -> int:
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+# --------------------------------------------------------------------------
+# clocks during the timed region (NVML through ctypes; nvidia-smi fallback)
+# --------------------------------------------------------------------------
+
+REASON_BITS = [(0x1, "gpu_idle"), (0x2, "applications_clocks_setting"), (0x4, "sw_power_cap"),
+               (0x8, "hw_slowdown"), (0x10, "sync_boost"), (0x20, "sw_thermal_slowdown"),
+               (0x40, "hw_thermal_slowdown"), (0x80, "hw_power_brake_slowdown"),
+               (0x100, "display_clock_setting")]
+
+
+class ClockSampler:
+    """Samples the SM clock and the clock-event reasons while running."""
+
+    def __init__(self, torch_device: int, interval_s: float = 0.002):
+        self.interval = interval_s
+        self.samples = []
+        self.max_mhz = None
+        self.source = None
+        self._stop = threading.Event()
+        self._thread = None
+        self._proc = None
+        self._nvml = None
+        try:
+            self._init_nvml(torch_device)
+            self.source = "nvml"
+        except Exception:
+            self._nvml = None
+            self.source = "nvidia-smi"
+
+    def _init_nvml(self, torch_device):
+        lib = ctypes.CDLL("libnvidia-ml.so.1")
+        if lib.nvmlInit_v2() != 0:
+            raise RuntimeError("nvmlInit failed")
+        count = ctypes.c_uint()
+        lib.nvmlDeviceGetCount_v2(ctypes.byref(count))
+        handle = ctypes.c_void_p()
+        index = 0
+        try:
+            want = str(torch.cuda.get_device_properties(torch_device).uuid).lower().replace("gpu-", "")
+            buf = ctypes.create_string_buffer(96)
+            for i in range(count.value):
+                h = ctypes.c_void_p()
+                lib.nvmlDeviceGetHandleByIndex_v2(i, ctypes.byref(h))
+                lib.nvmlDeviceGetUUID(h, buf, 96)
+                if buf.value.decode().lower().replace("gpu-", "") == want:
+                    index = i
+                    break
+        except Exception:
+            index = 0
+        if lib.nvmlDeviceGetHandleByIndex_v2(index, ctypes.byref(handle)) != 0:
+            raise RuntimeError("no NVML handle")
+        mx = ctypes.c_uint()
+        lib.nvmlDeviceGetMaxClockInfo(handle, 1, ctypes.byref(mx))  # 1 = SM clock
+        self.max_mhz = mx.value
+        self._reasons_fn = getattr(lib, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            getattr(lib, "nvmlDeviceGetCurrentClocksThrottleReasons")
+        self._nvml, self._handle = lib, handle
+
+    def _loop(self):
+        lib, h = self._nvml, self._handle
+        clk, rs = ctypes.c_uint(), ctypes.c_ulonglong()
+        while not self._stop.is_set():
+            if lib.nvmlDeviceGetClockInfo(h, 1, ctypes.byref(clk)) == 0:
+                self._reasons_fn(h, ctypes.byref(rs))
+                self.samples.append((clk.value, rs.value))
+            time.sleep(self.interval)
+
+    def start(self):
+        if self._nvml is not None:
+            self._thread = threading.Thread(target=self._loop, daemon=True)
+            self._thread.start()
+        else:
+            try:
+                self._proc = subprocess.Popen(
+                    ["nvidia-smi", "--query-gpu=clocks.sm,clocks.max.sm,clocks_event_reasons.active",
+                     "--format=csv,noheader,nounits", "-lms", "100"],
+                    stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            except Exception:
+                self._proc = None
+
+    def stop(self) -> dict:
+        if self._thread is not None:
+            self._stop.set()
+            self._thread.join()
+        elif self._proc is not None:
+            self._proc.terminate()
+            out, _ = self._proc.communicate()
+            for line in out.splitlines():
+                parts = [p.strip() for p in line.split(",")]
+                try:
+                    self.samples.append((int(parts[0]), int(parts[2], 16)))
+                    self.max_mhz = int(parts[1])
+                except (ValueError, IndexError):
+                    pass
+        mhz = [s for s, _ in self.samples]
+        mask = 0
+        for _, r in self.samples:
+            mask |= r
+        reasons = [name for bit, name in REASON_BITS if mask & bit]
+        return {"sm_mhz": float(statistics.median(mhz)) if mhz else None,
+                "sm_max_mhz": self.max_mhz, "reasons": reasons, "samples": len(mhz),
+                "source": self.source}
+
+
+# --------------------------------------------------------------------------
+# distributed plumbing (timing only; the data path has no collective)
+# --------------------------------------------------------------------------
+
+def dist_env():
+    return (int(os.environ.get("WORLD_SIZE", "1")), int(os.environ.get("RANK", "0")),
+            int(os.environ.get("LOCAL_RANK", "0")))
+
+
+def reduce_timing(elapsed_s: float, units: float, world: int, device=None):
+    """Max of the ranks' elapsed times and the sum of their work units."""
+    if world == 1:
+        return elapsed_s, units
+    import torch.distributed as dist
+    t = torch.tensor([elapsed_s], dtype=torch.float64, device=device)
+    u = torch.tensor([units], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    dist.all_reduce(u, op=dist.ReduceOp.SUM)
+    return float(t.item()), float(u.item())
+
+
+def barrier(world: int):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+# --------------------------------------------------------------------------
+# CPU oracle timing (the reference arm and the cpu_baseline leg)
+# --------------------------------------------------------------------------
+
+def oracle_sample(w, x, r1, r2, g, tokens: int):
+    """The first `tokens` positions of batch 0 of a workload (a contiguous
+    sub-tensor of the same shape family)."""
+    xs = np.ascontiguousarray(x[:1, :tokens])
+    gs = np.ascontiguousarray(g[:1, :tokens])
+    c = np.ascontiguousarray(r1[:1, :tokens] if r1.shape[1] > 1 else r1[:1])
+    s = np.ascontiguousarray(r2[:1, :tokens] if r2.shape[1] > 1 else r2[:1])
+    return xs, c, s, gs
+
+
+def oracle_step(pool, cores, xs, c, s, gs, w):
+    """One step of the oracle on a sample: forward over x, backward over
+    grad, the tokens split across `cores` threads (the oracle's C calls
+    release the GIL; the oracle itself is unchanged)."""
+    import oracle
+    T = xs.shape[1]
+    cuts = np.linspace(0, T, cores + 1).astype(int)
+    parts = [(a, b) for a, b in zip(cuts[:-1], cuts[1:]) if b > a]
+
+    def run(args):
+        fn, arr, a, b = args
+        cc = c[:, a:b] if c.shape[1] > 1 else c
+        ss = s[:, a:b] if s.shape[1] > 1 else s
+        return fn(arr[:, a:b], cc, ss, w.dtype, w.start, w.end)
+
+    list(pool.map(run, [(oracle.fwd, xs, a, b) for a, b in parts]))
+    list(pool.map(run, [(oracle.bwd, gs, a, b) for a, b in parts]))
+
+
+def sample_bytes(w, tokens: int, r_tokens: int) -> int:
+    e = synth.ELEM_BYTES[w.dtype]
+    N = w.shape[2]
+    return 2 * 2 * tokens * N * w.L * e + 2 * 2 * r_tokens * w.L * e  # fwd + bwd
+
+
+def time_oracle(w, x, r1, r2, g, steps: int, warmup: int, budget_s: float):
+    import oracle
+    oracle.build()
+    cores = host_cores()
+    tokens = w.shape[1]  # batch 0: a quarter of the large workload
+    xs, c, s, gs = oracle_sample(w, x, r1, r2, g, tokens)
+    with ThreadPoolExecutor(max_workers=cores) as pool:
+        t0 = time.perf_counter()
+        oracle_step(pool, cores, xs, c, s, gs, w)
+        one = time.perf_counter() - t0
+        if one * (steps + warmup) > budget_s:  # shrink the sample to fit the budget
+            tokens = max(64, int(tokens * budget_s / (one * (steps + warmup))))
+            xs, c, s, gs = oracle_sample(w, x, r1, r2, g, tokens)
+        for _ in range(max(0, warmup - 1)):
+            oracle_step(pool, cores, xs, c, s, gs, w)
+        times = []
+        for _ in range(steps):
+            t0 = time.perf_counter()
+            oracle_step(pool, cores, xs, c, s, gs, w)
+            times.append(time.perf_counter() - t0)
+    r_tok = tokens if c.shape[1] > 1 else 1
+    per_step = sample_bytes(w, tokens, r_tok)
+    total = sum(times)
+    sample = (f"forward + backward of the CPU oracle over batch 0, positions [0, {tokens}) of the "
+              f"{w.name} workload ({tokens} x {w.shape[2]} rows of {w.L} {w.dtype} lanes), tokens "
+              f"split across {cores} threads; {steps} steps")
+    return {"value": per_step * steps / total / 1e9, "unit": "GB/s", "cores": cores,
+            "kind": "oracle", "sample": sample, "ms_per_step": 1e3 * total / steps}
+
+
+# --------------------------------------------------------------------------
+# the GPU arm
+# --------------------------------------------------------------------------
+
+def workload_config(w) -> dict:
+    return {"workload": f"{w.name}: {w.description}; one step = forward on x then backward on "
+                        f"grad (2 launches)",
+            "x_shape": list(w.shape), "partial_slice": [w.start, w.end], "r_shape": list(w.r_shape),
+            "algorithmic_bytes_per_launch": w.algorithmic_bytes(),
+            "l2": "inputs larger than L2 (x and grad 537 MB each, 129 MB L2): no flush between steps",
+            "parallelism": "one independent copy of the workload per GPU"}
+
+
+def l2_flusher(device):
+    size = torch.cuda.get_device_properties(device).L2_cache_size
+    buf = torch.empty(int(2.5 * size) // 4 + 1, dtype=torch.float32, device=device)
+    return lambda: buf.fill_(1.0)
+
+
+def time_launches(fn, n: int, flush=None):
+    """Median device time (s) of n launches, each bracketed by its own events;
+    the L2 flush (if any) runs outside the events."""
+    evs = []
+    for _ in range(n):
+        if flush is not None:
+            flush()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        fn()
+        b.record()
+        evs.append((a, b))
+    torch.cuda.synchronize()
+    return statistics.median(a.elapsed_time(b) for a, b in evs) / 1e3
+
+
+def breakdown(device, peak):
+    """Per named workload: cold (L2-flushed) device time and GB/s of each
+    direction, the configs the operator is specified on."""
+    from place_partial_rope_gb300 import binding
+    flush = l2_flusher(device)
+    out = {}
+    for name, w in synth.WORKLOADS.items():
+        x, r1, r2, g = synth.workload_inputs(w)
+        xd = synth.to_torch(x, w.dtype).to(device)
+        c = synth.to_torch(r1, w.dtype).to(device)
+        s = synth.to_torch(r2, w.dtype).to(device)
+        entry = {}
+        for d in w.directions:
+            buf = xd if d == "fwd" else synth.to_torch(g, w.dtype).to(device)
+            fn = binding.rope_partial_inplace_fwd if d == "fwd" else binding.rope_partial_inplace_bwd
+            call = (lambda fn=fn, buf=buf: fn(buf, c, s, w.start, w.end))
+            for _ in range(3):
+                call()
+            t = time_launches(call, 30, flush)
+            gbs = w.algorithmic_bytes() / t / 1e9
+            entry[d] = {"us": round(t * 1e6, 2), "GB/s": round(gbs, 1), "frac": round(gbs / peak, 4)}
+        out[name] = entry
+        del xd, c, s
+    torch.cuda.empty_cache()
+    return out
+
+
+def gpu_arm(args):
+    world, rank, local = dist_env()
+    from place_partial_rope_gb300 import binding, build
+    build.build()  # no-op when the in-tree library is current
+    lib = binding.load_library()
+    device = torch.device("cuda", local)
+    torch.cuda.set_device(device)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=device)
+
+    w = synth.WORKLOADS[HEADLINE]
+    peak, peak_kind = hbm_peak()
+    x, r1, r2, g = synth.workload_inputs(w)
+    xd = synth.to_torch(x, w.dtype).to(device)
+    gd = synth.to_torch(g, w.dtype).to(device)
+    c = synth.to_torch(r1, w.dtype).to(device)
+    s = synth.to_torch(r2, w.dtype).to(device)
+    plan = binding.rope_partial_plan(xd, c, s, w.start, w.end)
+    stream = torch.cuda.current_stream(device)
+
+    def fwd():
+        binding.rope_partial_inplace_fwd(xd, c, s, w.start, w.end)
+
+    def bwd():
+        binding.rope_partial_inplace_bwd(gd, c, s, w.start, w.end)
+
+    for _ in range(args.warmup):
+        fwd()
+        bwd()
+    K = args.steps
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(2 * K + 1)]
+    sampler = ClockSampler(local)
+    barrier(world)
+    torch.cuda.synchronize(device)
+    sampler.start()
+    ev[0].record(stream)
+    for i in range(K):
+        fwd()
+        ev[2 * i + 1].record(stream)
+        bwd()
+        ev[2 * i + 2].record(stream)
+    torch.cuda.synchronize(device)
+    clocks = sampler.stop()
+    barrier(world)
+
+    elapsed = ev[0].elapsed_time(ev[2 * K]) / 1e3
+    fwd_t = [ev[2 * i].elapsed_time(ev[2 * i + 1]) / 1e3 for i in range(K)]
+    bwd_t = [ev[2 * i + 1].elapsed_time(ev[2 * i + 2]) / 1e3 for i in range(K)]
+    per_launch = w.algorithmic_bytes()
+    bytes_step = 2 * per_launch
+    max_elapsed, total_bytes = reduce_timing(elapsed, bytes_step * K, world, device)
+    value = total_bytes / max_elapsed / 1e9
+
+    # the dominant kernel: the direction with the larger share of the time
+    dom, times = ("fwd", fwd_t) if sum(fwd_t) >= sum(bwd_t) else ("bwd", bwd_t)
+    kname = kernel_name(plan, w.dtype, 0 if dom == "fwd" else 1)
+    avg = sum(times) / len(times)
+    achieved = per_launch / avg / 1e9
+    traffic = stored_traffic(kname, w.name)
+    roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                "frac": round(achieved / peak, 4), "traffic": traffic,
+                "peak_source": f"{peak_kind} (HBM copy bandwidth, MEASURED_PEAKS.json hbm_gbs)"
+                if peak_kind == "measured" else "fallback 6.8 TB/s",
+                "kernel": kname, "kernel_avg_us": round(avg * 1e6, 2),
+                "fwd_avg_us": round(1e6 * sum(fwd_t) / K, 2),
+                "bwd_avg_us": round(1e6 * sum(bwd_t) / K, 2),
+                "algorithmic_bytes_per_launch": per_launch,
+                "traffic_note": "dram bytes per launch from the committed ncu summary of the same "
+                                "kernel sources" if traffic else
+                                "no ncu summary for the current kernel sources"}
+
+    e2e = e2e_measure(w, x, r1, r2, g, device, min(K, 20), binding)
+    out = {"metric": METRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": world,
+           "steps": K, "warmup": args.warmup, "ms_per_step": round(1e3 * max_elapsed / K, 5),
+           "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "fp32",
+           "data": "synthetic: seeded N(0,1) activations and gradients, base-10000 cos/sin table "
+                   "at seeded per-batch position offsets",
+           "config": workload_config(w),
+           "frac_of_peak": round(value / world / peak, 4),
+           "gelem_per_s": round(2 * w.slice_elems() * K * world / max_elapsed / 1e9, 2),
+           "roofline": roofline, "e2e": e2e, "gpu_launches": 2 * K * int(plan.launches),
+           "clocks": clocks,
+           "plan": {"vec_bytes": plan.vec_bytes, "heads_per_thread": plan.heads_per_thread,
+                    "blocks": plan.blocks, "threads_per_block": plan.threads_per_block,
+                    "launches_per_call": plan.launches}}
+    if rank == 0:
+        out["workloads"] = breakdown(device, peak)
+    if rank == 0 and world == 1:
+        out["cpu_baseline"] = time_oracle(w, x, r1, r2, g, steps=20, warmup=1, budget_s=60.0)
+        out["cpu_baseline"].pop("ms_per_step", None)
+    if rank == 0:
+        print(json.dumps(out), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    _ = lib
+    return 0
+
+
+def e2e_measure(w, x, r1, r2, g, device, steps: int, binding):
+    """The same metric through the C ABI with host buffers: every step copies
+    x, grad, cos and sin from pinned host memory, runs the forward and the
+    backward, and reads x and grad back into pinned host memory."""
+    hx = synth.to_torch(x, w.dtype).pin_memory()
+    hg = synth.to_torch(g, w.dtype).pin_memory()
+    hc = synth.to_torch(r1, w.dtype).pin_memory()
+    hs = synth.to_torch(r2, w.dtype).pin_memory()
+    ox, og = torch.empty_like(hx).pin_memory(), torch.empty_like(hg).pin_memory()
+    dx, dg = torch.empty_like(hx, device=device), torch.empty_like(hg, device=device)
+    dc, ds = torch.empty_like(hc, device=device), torch.empty_like(hs, device=device)
+
+    def step():
+        dx.copy_(hx, non_blocking=True)
+        dg.copy_(hg, non_blocking=True)
+        dc.copy_(hc, non_blocking=True)
+        ds.copy_(hs, non_blocking=True)
+        binding.rope_partial_inplace_fwd(dx, dc, ds, w.start, w.end)
+        binding.rope_partial_inplace_bwd(dg, dc, ds, w.start, w.end)
+        ox.copy_(dx, non_blocking=True)
+        og.copy_(dg, non_blocking=True)
+
+    step()
+    torch.cuda.synchronize(device)
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    for _ in range(steps):
+        step()
+    b.record()
+    torch.cuda.synchronize(device)
+    t = a.elapsed_time(b) / 1e3 / steps
+    h2d = hx.nbytes + hg.nbytes + hc.nbytes + hs.nbytes
+    d2h = ox.nbytes + og.nbytes
+    return {"value": round(2 * w.algorithmic_bytes() / t / 1e9, 2), "unit": "GB/s",
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": steps,
+            "ms_per_step": round(t * 1e3, 3),
+            "path": "pinned host -> device copies of x, grad, cos, sin; forward; backward; "
+                    "x and grad back to pinned host (one stream)"}
+
+
+def reference_arm(args):
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return 0
+    w = synth.WORKLOADS[HEADLINE]
+    x, r1, r2, g = synth.workload_inputs(w)
+    base = time_oracle(w, x, r1, r2, g, steps=args.steps, warmup=args.warmup, budget_s=150.0)
+    out = {"impl": "reference", "metric": METRIC, "value": round(base["value"], 4), "unit": "GB/s",
+           "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+           "ms_per_step": round(base["ms_per_step"], 3), "higher_is_better": True,
+           "scaling": "weak", "vs_baseline": None, "dtype": "fp32",
+           "data": "synthetic: seeded N(0,1) activations and gradients, base-10000 cos/sin table",
+           "config": workload_config(w),
+           "cpu_baseline": {k: base[k] for k in ("value", "unit", "cores", "kind", "sample")},
+           "e2e": {"value": round(base["value"], 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                   "d2h_bytes_per_step": 0}}
+    out["cpu_baseline"]["value"] = out["value"]
+    print(json.dumps(out), flush=True)
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=500)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["native", "reference"], default="native")
+    args = ap.parse_args()
+    if args.warmup < 3 and args.impl == "native":
+        args.warmup = 3
+    if args.impl == "reference":
+        return reference_arm(args)
+    return gpu_arm(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -121,7 +121,7 @@ def test_noops_leave_memory_untouched(dtype):
     torch.cuda.synchronize()
     assert_same(synth.from_torch(xd), x, dtype, "start == end")
     e = torch.empty((0, 3, 4, 16), dtype=xd.dtype, device=DEV)
-    c = to_dev(r1, dtype)
+    c = to_dev(r1[:1], dtype)  # batch dim 1 broadcasts against B == 0
     binding.rope_partial_inplace_fwd(e, c, c, 0, 8)
     binding.rope_partial_inplace_bwd(e, c, c, 0, 8)
     torch.cuda.synchronize()
