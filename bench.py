@@ -321,14 +321,24 @@ def workload_config(w) -> dict:
 
 
 def l2_flusher(device):
+    """Flush L2 without leaving it dirty: write a buffer 2.5x the L2 size,
+    then read another of that size, so the next kernel starts with none of
+    its own lines cached and pays no write-back of the flush's lines."""
     size = torch.cuda.get_device_properties(device).L2_cache_size
-    buf = torch.empty(int(2.5 * size) // 4 + 1, dtype=torch.float32, device=device)
-    return lambda: buf.fill_(1.0)
+    n = int(2.5 * size) // 4 + 1
+    wbuf = torch.empty(n, dtype=torch.float32, device=device)
+    rbuf = torch.ones(n, dtype=torch.float32, device=device)
+
+    def flush():
+        wbuf.fill_(1.0)
+        torch.sum(rbuf)
+    return flush
 
 
 def time_launches(fn, n: int, flush=None):
     """Median device time (s) of n launches, each bracketed by its own events;
-    the L2 flush (if any) runs outside the events."""
+    the L2 flush (if any) runs outside the events and keeps the GPU busy
+    while the host queues the launch."""
     evs = []
     for _ in range(n):
         if flush is not None:
@@ -342,29 +352,69 @@ def time_launches(fn, n: int, flush=None):
     return statistics.median(a.elapsed_time(b) for a, b in evs) / 1e3
 
 
+def time_back_to_back(fn, n: int):
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    for _ in range(n):
+        fn()
+    b.record()
+    torch.cuda.synchronize()
+    return a.elapsed_time(b) / 1e3 / n
+
+
+def time_graph(make_call, n: int, reps: int = 5):
+    """Per-launch time of n launches captured in one CUDA graph and replayed
+    (no host launch cost; the data stays in L2 when it fits)."""
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        call = make_call()  # marshalled on the capture stream
+        for _ in range(n):
+            call()
+    g.replay()
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    for _ in range(reps):
+        g.replay()
+    b.record()
+    torch.cuda.synchronize()
+    return a.elapsed_time(b) / 1e3 / (n * reps)
+
+
 def breakdown(device, peak):
-    """Per named workload: cold (L2-flushed) device time and GB/s of each
-    direction, the configs the operator is specified on."""
+    """Per named workload and direction: cold (L2-flushed) device time per
+    launch, GB/s and fraction of peak; steady back-to-back time where the
+    bytes a launch touches exceed twice the L2; and the per-launch time of a
+    replayed CUDA graph of 20 launches."""
     from place_partial_rope_gb300 import binding
     flush = l2_flusher(device)
+    l2 = torch.cuda.get_device_properties(device).L2_cache_size
     out = {}
     for name, w in synth.WORKLOADS.items():
         x, r1, r2, g = synth.workload_inputs(w)
         xd = synth.to_torch(x, w.dtype).to(device)
+        gd = synth.to_torch(g, w.dtype).to(device) if g is not None else None
         c = synth.to_torch(r1, w.dtype).to(device)
         s = synth.to_torch(r2, w.dtype).to(device)
         entry = {}
         for d in w.directions:
-            buf = xd if d == "fwd" else synth.to_torch(g, w.dtype).to(device)
-            fn = binding.rope_partial_inplace_fwd if d == "fwd" else binding.rope_partial_inplace_bwd
-            call = (lambda fn=fn, buf=buf: fn(buf, c, s, w.start, w.end))
+            buf = xd if d == "fwd" else gd
+            prep = binding.prepare_fwd if d == "fwd" else binding.prepare_bwd
+            call = prep(buf, c, s, w.start, w.end)
             for _ in range(3):
                 call()
             t = time_launches(call, 30, flush)
             gbs = w.algorithmic_bytes() / t / 1e9
-            entry[d] = {"us": round(t * 1e6, 2), "GB/s": round(gbs, 1), "frac": round(gbs / peak, 4)}
+            e = {"cold_us": round(t * 1e6, 2), "cold_GB/s": round(gbs, 1),
+                 "cold_frac": round(gbs / peak, 4)}
+            if w.algorithmic_bytes() > 2 * l2:
+                tb = time_back_to_back(call, 30)
+                e["steady_us"] = round(tb * 1e6, 2)
+                e["steady_frac"] = round(w.algorithmic_bytes() / tb / 1e9 / peak, 4)
+            e["graph_us"] = round(time_graph(lambda: prep(buf, c, s, w.start, w.end), 20) * 1e6, 2)
+            entry[d] = e
         out[name] = entry
-        del xd, c, s
+        del xd, gd, c, s
     torch.cuda.empty_cache()
     return out
 
@@ -390,11 +440,10 @@ def gpu_arm(args):
     plan = binding.rope_partial_plan(xd, c, s, w.start, w.end)
     stream = torch.cuda.current_stream(device)
 
-    def fwd():
-        binding.rope_partial_inplace_fwd(xd, c, s, w.start, w.end)
-
-    def bwd():
-        binding.rope_partial_inplace_bwd(gd, c, s, w.start, w.end)
+    # arguments marshalled once: one ctypes call (about 4 us of host time)
+    # per launch, far below the ~100 us a launch of this workload takes
+    fwd = binding.prepare_fwd(xd, c, s, w.start, w.end)
+    bwd = binding.prepare_bwd(gd, c, s, w.start, w.end)
 
     for _ in range(args.warmup):
         fwd()
@@ -481,13 +530,16 @@ def e2e_measure(w, x, r1, r2, g, device, steps: int, binding):
     dx, dg = torch.empty_like(hx, device=device), torch.empty_like(hg, device=device)
     dc, ds = torch.empty_like(hc, device=device), torch.empty_like(hs, device=device)
 
+    fwd = binding.prepare_fwd(dx, dc, ds, w.start, w.end)
+    bwd = binding.prepare_bwd(dg, dc, ds, w.start, w.end)
+
     def step():
         dx.copy_(hx, non_blocking=True)
         dg.copy_(hg, non_blocking=True)
         dc.copy_(hc, non_blocking=True)
         ds.copy_(hs, non_blocking=True)
-        binding.rope_partial_inplace_fwd(dx, dc, ds, w.start, w.end)
-        binding.rope_partial_inplace_bwd(dg, dc, ds, w.start, w.end)
+        fwd()
+        bwd()
         ox.copy_(dx, non_blocking=True)
         og.copy_(dg, non_blocking=True)
 

@@ -134,6 +134,38 @@ def rope_partial_inplace_bwd(grad: torch.Tensor, r1: torch.Tensor, r2: torch.Ten
     _call("rope_partial_inplace_bwd", grad, r1, r2, start, end, stream)
 
 
+class PreparedCall:
+    """One forward or backward call with its arguments marshalled once.
+
+    Calling the object launches the kernel again on the same tensors and
+    stream (for loops that launch the same call many times, where per-call
+    marshalling would cost more host time than the kernel takes).  It keeps
+    references to the tensors so their memory stays alive.
+    """
+
+    def __init__(self, name: str, x, r1, r2, start: int, end: int, stream=None):
+        self._lib = load_library()
+        self._fn = getattr(self._lib, name)
+        self._keep = (x, r1, r2)
+        self._args = (*_marshal(x, r1, r2), int(start), int(end),
+                      _stream_handle(stream, x.device))
+
+    def __call__(self) -> None:
+        st = self._fn(*self._args)
+        if st != ROPE_OK:
+            _raise_for(self._lib, st)
+
+
+def prepare_fwd(x, r1, r2, start: int, end: int, stream=None) -> PreparedCall:
+    """``rope_partial_inplace_fwd`` with its arguments marshalled once."""
+    return PreparedCall("rope_partial_inplace_fwd", x, r1, r2, start, end, stream)
+
+
+def prepare_bwd(grad, r1, r2, start: int, end: int, stream=None) -> PreparedCall:
+    """``rope_partial_inplace_bwd`` with its arguments marshalled once."""
+    return PreparedCall("rope_partial_inplace_bwd", grad, r1, r2, start, end, stream)
+
+
 def rope_partial_plan(x: torch.Tensor, r1: torch.Tensor, r2: torch.Tensor, start: int, end: int,
                       sm_count: int = 0) -> RopePlan:
     """The launch plan the forward would use (no launch).  Works on CPU

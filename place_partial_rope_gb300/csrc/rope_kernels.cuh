@@ -102,17 +102,25 @@ struct Pack<__half> {
 // (read-only for the whole kernel, so they may take the non-coherent path)
 // ------------------------------------------------------------------------
 
+// x loads carry an explicit 64-byte L2 prefetch size.  Without it a miss
+// pulls the whole 128-byte line from HBM; a slice that ends a few bytes into
+// a line (e.g. bytes [136, 392) of a 512-byte row) then reads up to 120
+// bytes it never uses.  64 bytes is the HBM access atom, so nothing smaller
+// can be fetched anyway.  The asm is volatile so the U loads keep their
+// order; each store depends on its own load's data, which orders them.
 template <int W>
 __device__ __forceinline__ Words<W> ld_vec(const char* p) {
     Words<W> v;
     if constexpr (W == 4) {
-        const uint4 q = *reinterpret_cast<const uint4*>(p);
-        v.w[0] = q.x; v.w[1] = q.y; v.w[2] = q.z; v.w[3] = q.w;
+        asm volatile("ld.global.L2::64B.v4.u32 {%0, %1, %2, %3}, [%4];"
+                     : "=r"(v.w[0]), "=r"(v.w[1]), "=r"(v.w[2]), "=r"(v.w[3])
+                     : "l"(p));
     } else if constexpr (W == 2) {
-        const uint2 q = *reinterpret_cast<const uint2*>(p);
-        v.w[0] = q.x; v.w[1] = q.y;
+        asm volatile("ld.global.L2::64B.v2.u32 {%0, %1}, [%2];"
+                     : "=r"(v.w[0]), "=r"(v.w[1])
+                     : "l"(p));
     } else {
-        v.w[0] = *reinterpret_cast<const uint32_t*>(p);
+        asm volatile("ld.global.L2::64B.u32 %0, [%1];" : "=r"(v.w[0]) : "l"(p));
     }
     return v;
 }
