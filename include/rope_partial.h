@@ -29,7 +29,7 @@
  * deterministic: no atomics, no reductions.
  *
  * Memory: every pointer is a device pointer (or managed memory) on the
- * current CUDA device.  The caller owns every buffer; the library allocates
+ * current CUDA device; the *_host entry points below take host buffers.  The caller owns every buffer; the library allocates
  * nothing and needs no workspace.  Calls are asynchronous on `stream` and
  * never synchronise.
  *
@@ -112,6 +112,38 @@ rope_status_t rope_partial_inplace_bwd(void* grad, const void* r1, const void* r
                                        const int64_t r1_shape[4], const int64_t r1_stride[4],
                                        const int64_t r2_shape[4], const int64_t r2_stride[4],
                                        int64_t start, int64_t end, rope_stream_t stream);
+
+/*
+ * rope_partial_inplace_fwd_host / rope_partial_inplace_bwd_host -- the same
+ * operations on buffers in HOST memory, which the kernel reads and writes in
+ * place across the host link (zero copy: no device buffer, no staging copy).
+ * On Grace-Blackwell the GPU reaches host memory coherently over NVLink-C2C,
+ * so only the slice bytes and the cos/sin rows cross the link, instead of
+ * whole tensors copied both ways.
+ *
+ * Arguments and layout are those of rope_partial_inplace_fwd / _bwd.  x (or
+ * grad), r1 and r2 must be memory the current device can access: page-locked
+ * host memory (cudaHostAlloc / cudaMallocHost, or registered with
+ * cudaHostRegister), managed memory, device memory, or -- on a device that
+ * reports cudaDevAttrPageableMemoryAccess -- any host memory.  The first and
+ * last byte of each buffer are checked with cudaPointerGetAttributes before
+ * anything is launched; a buffer the device cannot reach returns
+ * ROPE_ERR_INVALID.  The call is asynchronous: synchronise `stream` before
+ * the host reads x.
+ */
+rope_status_t rope_partial_inplace_fwd_host(void* x, const void* r1, const void* r2,
+                                            rope_dtype_t dtype, int64_t B, int64_t S,
+                                            int64_t N, int64_t D,
+                                            const int64_t r1_shape[4], const int64_t r1_stride[4],
+                                            const int64_t r2_shape[4], const int64_t r2_stride[4],
+                                            int64_t start, int64_t end, rope_stream_t stream);
+
+rope_status_t rope_partial_inplace_bwd_host(void* grad, const void* r1, const void* r2,
+                                            rope_dtype_t dtype, int64_t B, int64_t S,
+                                            int64_t N, int64_t D,
+                                            const int64_t r1_shape[4], const int64_t r1_stride[4],
+                                            const int64_t r2_shape[4], const int64_t r2_stride[4],
+                                            int64_t start, int64_t end, rope_stream_t stream);
 
 /* A static, human-readable name of a status code. */
 const char* rope_status_str(rope_status_t status);

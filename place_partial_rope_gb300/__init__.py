@@ -12,7 +12,8 @@ Submodules:
 from __future__ import annotations
 
 _BINDING_NAMES = (
-    "rope_partial_inplace_fwd", "rope_partial_inplace_bwd", "RopeError", "load_library",
+    "rope_partial_inplace_fwd", "rope_partial_inplace_bwd", "rope_partial_inplace_fwd_host",
+    "rope_partial_inplace_bwd_host", "prepare_fwd", "prepare_bwd", "RopeError", "load_library",
     "library_path",
 )
 

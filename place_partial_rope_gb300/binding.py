@@ -6,6 +6,7 @@ library has not been built, loading raises -- there is no CPU fallback.
 
     rope_partial_inplace_fwd(x, r1, r2, start, end, stream=None)
     rope_partial_inplace_bwd(grad, r1, r2, start, end, stream=None)
+    rope_partial_inplace_fwd_host(...), rope_partial_inplace_bwd_host(...)   (host tensors)
 
 ``x`` / ``grad``: contiguous CUDA tensor (B, S, N, D) of bf16, fp16 or fp32,
 modified in place.  ``r1`` (cos) and ``r2`` (sin): 4-D CUDA tensors of the
@@ -63,7 +64,8 @@ def load_library() -> ctypes.CDLL:
     args = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int, ctypes.c_int64,
             ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, i64p, i64p, i64p, i64p,
             ctypes.c_int64, ctypes.c_int64]
-    for name in ("rope_partial_inplace_fwd", "rope_partial_inplace_bwd"):
+    for name in ("rope_partial_inplace_fwd", "rope_partial_inplace_bwd",
+                 "rope_partial_inplace_fwd_host", "rope_partial_inplace_bwd_host"):
         fn = getattr(lib, name)
         fn.restype = ctypes.c_int
         fn.argtypes = args + [ctypes.c_void_p]
@@ -96,7 +98,7 @@ def _stream_handle(stream, device) -> int:
     return int(stream)
 
 
-def _marshal(x: torch.Tensor, r1: torch.Tensor, r2: torch.Tensor):
+def _marshal(x: torch.Tensor, r1: torch.Tensor, r2: torch.Tensor, host: bool = False):
     if x.dim() != 4:
         raise RopeError(ROPE_ERR_INVALID, f"x must be 4-D (B, S, N, D), got {x.dim()}-D")
     if r1.dim() != 4 or r2.dim() != 4:
@@ -108,7 +110,9 @@ def _marshal(x: torch.Tensor, r1: torch.Tensor, r2: torch.Tensor):
     if not x.is_contiguous():
         raise RopeError(ROPE_ERR_INVALID, "x must be contiguous")
     for t in (x, r1, r2):
-        if not t.is_cuda or t.device != x.device:
+        if host and t.is_cuda:
+            raise RopeError(ROPE_ERR_INVALID, "the *_host calls take CPU (host) tensors")
+        if not host and (not t.is_cuda or t.device != x.device):
             raise RopeError(ROPE_ERR_INVALID, "x, r1 and r2 must be CUDA tensors on one device")
     return (x.data_ptr(), r1.data_ptr(), r2.data_ptr(), DTYPE_CODE[x.dtype], *x.shape,
             _i64x4(r1.shape), _i64x4(r1.stride()), _i64x4(r2.shape), _i64x4(r2.stride()))
@@ -134,6 +138,30 @@ def rope_partial_inplace_bwd(grad: torch.Tensor, r1: torch.Tensor, r2: torch.Ten
     _call("rope_partial_inplace_bwd", grad, r1, r2, start, end, stream)
 
 
+def _call_host(name: str, x, r1, r2, start: int, end: int, stream=None) -> None:
+    lib = load_library()
+    margs = _marshal(x, r1, r2, host=True)
+    handle = stream.cuda_stream if isinstance(stream, torch.cuda.Stream) else (
+        torch.cuda.current_stream().cuda_stream if stream is None else int(stream))
+    st = getattr(lib, name)(*margs, int(start), int(end), handle)
+    _raise_for(lib, st)
+
+
+def rope_partial_inplace_fwd_host(x: torch.Tensor, r1: torch.Tensor, r2: torch.Tensor,
+                                  start: int, end: int, stream=None) -> None:
+    """Forward on host tensors, read and written in place by the GPU (zero
+    copy).  x, r1 and r2 are CPU tensors the current CUDA device can reach
+    (pinned memory, or any memory on devices with pageable-memory access).
+    Asynchronous: synchronise the stream before reading x on the host."""
+    _call_host("rope_partial_inplace_fwd_host", x, r1, r2, start, end, stream)
+
+
+def rope_partial_inplace_bwd_host(grad: torch.Tensor, r1: torch.Tensor, r2: torch.Tensor,
+                                  start: int, end: int, stream=None) -> None:
+    """Backward on host tensors (zero copy); see rope_partial_inplace_fwd_host."""
+    _call_host("rope_partial_inplace_bwd_host", grad, r1, r2, start, end, stream)
+
+
 class PreparedCall:
     """One forward or backward call with its arguments marshalled once.
 
@@ -147,8 +175,10 @@ class PreparedCall:
         self._lib = load_library()
         self._fn = getattr(self._lib, name)
         self._keep = (x, r1, r2)
-        self._args = (*_marshal(x, r1, r2), int(start), int(end),
-                      _stream_handle(stream, x.device))
+        host = name.endswith("_host")
+        dev = torch.device("cuda", torch.cuda.current_device()) if host else x.device
+        self._args = (*_marshal(x, r1, r2, host=host), int(start), int(end),
+                      _stream_handle(stream, dev))
 
     def __call__(self) -> None:
         st = self._fn(*self._args)
@@ -164,6 +194,16 @@ def prepare_fwd(x, r1, r2, start: int, end: int, stream=None) -> PreparedCall:
 def prepare_bwd(grad, r1, r2, start: int, end: int, stream=None) -> PreparedCall:
     """``rope_partial_inplace_bwd`` with its arguments marshalled once."""
     return PreparedCall("rope_partial_inplace_bwd", grad, r1, r2, start, end, stream)
+
+
+def prepare_fwd_host(x, r1, r2, start: int, end: int, stream=None) -> PreparedCall:
+    """``rope_partial_inplace_fwd_host`` with its arguments marshalled once."""
+    return PreparedCall("rope_partial_inplace_fwd_host", x, r1, r2, start, end, stream)
+
+
+def prepare_bwd_host(grad, r1, r2, start: int, end: int, stream=None) -> PreparedCall:
+    """``rope_partial_inplace_bwd_host`` with its arguments marshalled once."""
+    return PreparedCall("rope_partial_inplace_bwd_host", grad, r1, r2, start, end, stream)
 
 
 def rope_partial_plan(x: torch.Tensor, r1: torch.Tensor, r2: torch.Tensor, start: int, end: int,

@@ -220,15 +220,37 @@ int64_t grid_for(int64_t tasks, int64_t sms, int64_t blocks_per_sm) {
     return need < resident ? need : resident;
 }
 
+// Bytes spanned by a cos/sin tensor: the farthest row plus one row.
+int64_t r_extent(const Resolved& R, int r, const int64_t* shape) {
+    int64_t far = 0;
+    for (int k = 0; k < 3; ++k) far += (shape[k] - 1) * R.rb[r][k];
+    return far + R.L * R.e;
+}
+
 rope_status_t run(int dir, void* x, const void* r1, const void* r2, int dtype, int64_t B,
                   int64_t S, int64_t N, int64_t D, const int64_t* r1_shape,
                   const int64_t* r1_stride, const int64_t* r2_shape, const int64_t* r2_stride,
-                  int64_t start, int64_t end, rope_stream_t stream) {
+                  int64_t start, int64_t end, rope_stream_t stream, bool host_buffers) {
     g_msg[0] = '\0';
     Resolved R;
     rope_status_t st = check(x, r1, r2, dtype, B, S, N, D, r1_shape, r1_stride, r2_shape,
                              r2_stride, start, end, &R);
     if (st != ROPE_OK || R.empty) return st;
+    if (host_buffers) {
+        // the kernel works on the host buffers in place: take the addresses
+        // the device uses for them, or refuse a buffer it cannot reach
+        const char* err = nullptr;
+        const void* dx = nullptr;
+        const void* d1 = nullptr;
+        const void* d2 = nullptr;
+        st = device_address(x, B * S * N * D * R.e, &dx, &err);
+        if (st == ROPE_OK) st = device_address(r1, r_extent(R, 0, r1_shape), &d1, &err);
+        if (st == ROPE_OK) st = device_address(r2, r_extent(R, 1, r2_shape), &d2, &err);
+        if (st != ROPE_OK) return fail(st, "host buffer: %s", err);
+        x = const_cast<void*>(dx);
+        r1 = d1;
+        r2 = d2;
+    }
     Plan P;
     st = make_plan(dir, dtype, x, r1, r2, N, D, start, R, &P);
     if (st != ROPE_OK) return st;
@@ -268,7 +290,7 @@ rope_status_t rope_partial_inplace_fwd(void* x, const void* r1, const void* r2,
                                        const int64_t r2_stride[4], int64_t start, int64_t end,
                                        rope_stream_t stream) {
     return rope::run(rope::kFwd, x, r1, r2, dtype, B, S, N, D, r1_shape, r1_stride, r2_shape,
-                     r2_stride, start, end, stream);
+                     r2_stride, start, end, stream, false);
 }
 
 rope_status_t rope_partial_inplace_bwd(void* grad, const void* r1, const void* r2,
@@ -278,7 +300,27 @@ rope_status_t rope_partial_inplace_bwd(void* grad, const void* r1, const void* r
                                        const int64_t r2_stride[4], int64_t start, int64_t end,
                                        rope_stream_t stream) {
     return rope::run(rope::kBwd, grad, r1, r2, dtype, B, S, N, D, r1_shape, r1_stride, r2_shape,
-                     r2_stride, start, end, stream);
+                     r2_stride, start, end, stream, false);
+}
+
+rope_status_t rope_partial_inplace_fwd_host(void* x, const void* r1, const void* r2,
+                                            rope_dtype_t dtype, int64_t B, int64_t S, int64_t N,
+                                            int64_t D, const int64_t r1_shape[4],
+                                            const int64_t r1_stride[4], const int64_t r2_shape[4],
+                                            const int64_t r2_stride[4], int64_t start,
+                                            int64_t end, rope_stream_t stream) {
+    return rope::run(rope::kFwd, x, r1, r2, dtype, B, S, N, D, r1_shape, r1_stride, r2_shape,
+                     r2_stride, start, end, stream, true);
+}
+
+rope_status_t rope_partial_inplace_bwd_host(void* grad, const void* r1, const void* r2,
+                                            rope_dtype_t dtype, int64_t B, int64_t S, int64_t N,
+                                            int64_t D, const int64_t r1_shape[4],
+                                            const int64_t r1_stride[4], const int64_t r2_shape[4],
+                                            const int64_t r2_stride[4], int64_t start,
+                                            int64_t end, rope_stream_t stream) {
+    return rope::run(rope::kBwd, grad, r1, r2, dtype, B, S, N, D, r1_shape, r1_stride, r2_shape,
+                     r2_stride, start, end, stream, true);
 }
 
 const char* rope_status_str(rope_status_t status) {

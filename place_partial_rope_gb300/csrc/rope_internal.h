@@ -50,6 +50,12 @@ struct Plan {
 rope_status_t launch_piece(const Plan& plan, const KernelArgs& args, uint32_t blocks,
                            rope_stream_t stream, const char** err);
 
+// A device address for the buffer [p, p + bytes) when the current device
+// can reach all of it (device, managed, page-locked host memory, or any host
+// memory on a device with pageable-memory access); ROPE_ERR_INVALID when it
+// cannot (defined in the .cu).
+rope_status_t device_address(const void* p, int64_t bytes, const void** out, const char** err);
+
 // The current device's SM count and the planned kernel's resident blocks
 // per SM (defined in the .cu; the only device queries the library makes).
 rope_status_t device_sm_count(int* sms, const char** err);

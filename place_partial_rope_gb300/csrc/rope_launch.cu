@@ -32,7 +32,56 @@ rope_status_t cuda_fail(cudaError_t e, const char** err) {
     return ROPE_ERR_CUDA;
 }
 
+// The address the current device uses to reach p (ROPE_ERR_INVALID when
+// it cannot reach p).
+rope_status_t resolve_one(const void* p, const void** out, const char** err) {
+    cudaPointerAttributes a;
+    cudaError_t e = cudaPointerGetAttributes(&a, p);
+    if (e != cudaSuccess) return cuda_fail(e, err);
+    switch (a.type) {
+        case cudaMemoryTypeDevice:
+        case cudaMemoryTypeManaged:
+            *out = p;
+            return ROPE_OK;
+        case cudaMemoryTypeHost:
+            if (a.devicePointer) {
+                *out = a.devicePointer;
+                return ROPE_OK;
+            }
+            *err = "page-locked host buffer is not mapped for the current device";
+            return ROPE_ERR_INVALID;
+        default: {  // unregistered (pageable) host memory
+            int dev = 0, pageable = 0;
+            e = cudaGetDevice(&dev);
+            if (e != cudaSuccess) return cuda_fail(e, err);
+            e = cudaDeviceGetAttribute(&pageable, cudaDevAttrPageableMemoryAccess, dev);
+            if (e != cudaSuccess) return cuda_fail(e, err);
+            if (pageable) {
+                *out = p;
+                return ROPE_OK;
+            }
+            *err = "pageable host buffer: this device cannot access it; use page-locked memory";
+            return ROPE_ERR_INVALID;
+        }
+    }
+}
+
 }  // namespace
+
+rope_status_t device_address(const void* p, int64_t bytes, const void** out, const char** err) {
+    const void* first = nullptr;
+    const void* last = nullptr;
+    rope_status_t st = resolve_one(p, &first, err);
+    if (st != ROPE_OK) return st;
+    st = resolve_one(static_cast<const char*>(p) + (bytes > 0 ? bytes - 1 : 0), &last, err);
+    if (st != ROPE_OK) return st;
+    if (static_cast<const char*>(last) - static_cast<const char*>(first) != (bytes > 0 ? bytes - 1 : 0)) {
+        *err = "buffer is not one contiguous device-accessible range";
+        return ROPE_ERR_INVALID;
+    }
+    *out = first;
+    return ROPE_OK;
+}
 
 rope_status_t device_sm_count(int* sms, const char** err) {
     int dev = 0;

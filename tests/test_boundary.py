@@ -60,8 +60,9 @@ def test_header_symbols_are_exported(lib):
     text = open(HEADER).read()
     text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
     names = set(re.findall(r"\b(rope_[a-z_]+)\s*\(", text))
-    assert names == {"rope_partial_inplace_fwd", "rope_partial_inplace_bwd", "rope_status_str",
-                     "rope_last_error_message", "rope_partial_plan"}
+    assert names == {"rope_partial_inplace_fwd", "rope_partial_inplace_bwd",
+                     "rope_partial_inplace_fwd_host", "rope_partial_inplace_bwd_host",
+                     "rope_status_str", "rope_last_error_message", "rope_partial_plan"}
     for n in names:
         assert hasattr(lib, n), n
     nm = subprocess.run(["nm", "-D", "--defined-only", binding.library_path()],
@@ -84,7 +85,11 @@ def test_status_strings(lib):
     assert lib.rope_status_str(99) == b"ROPE_ERR_UNKNOWN"
 
 
-@pytest.mark.parametrize("fn", ["rope_partial_inplace_fwd", "rope_partial_inplace_bwd"])
+ALL_FNS = ["rope_partial_inplace_fwd", "rope_partial_inplace_bwd", "rope_partial_inplace_fwd_host",
+           "rope_partial_inplace_bwd_host"]
+
+
+@pytest.mark.parametrize("fn", ALL_FNS)
 @pytest.mark.parametrize("kwargs,status,needle", [
     (dict(dtype=3), INVALID, "dtype"),
     (dict(dtype=-1), INVALID, "dtype"),
@@ -116,7 +121,7 @@ def test_rejected_calls(lib, fn, kwargs, status, needle):
     assert needle in lib.rope_last_error_message().decode()
 
 
-@pytest.mark.parametrize("fn", ["rope_partial_inplace_fwd", "rope_partial_inplace_bwd"])
+@pytest.mark.parametrize("fn", ALL_FNS)
 @pytest.mark.parametrize("kwargs", [
     dict(start=4, end=4, x=0, r1=0, r2=0),                      # empty slice, null pointers
     dict(start=0, end=0, x=0, r1=0, r2=0, r_shape="null", r2_shape="null",
