@@ -326,15 +326,15 @@ def time_oracle(w, x, r1, r2, g, steps: int, warmup: int, budget_s: float):
 # the GPU arm
 # --------------------------------------------------------------------------
 
-def workload_config(w) -> dict:
+def workload_config(w, l2_bytes: int = 132 * 2**20) -> dict:
     step = ("forward on x then backward on grad (2 launches)" if "bwd" in w.directions
             else "forward on x (1 launch)")
     xbytes = int(np.prod(w.shape)) * synth.ELEM_BYTES[w.dtype]
-    big = w.algorithmic_bytes() > 2 * 132 * 2**20
+    big = w.algorithmic_bytes() > 1.5 * l2_bytes
     l2 = (f"inputs larger than L2 ({xbytes / 1e6:.0f} MB per tensor, {w.algorithmic_bytes() / 1e6:.0f} "
-          f"MB touched per launch vs ~132 MB L2): no flush between steps" if big else
-          f"NOT larger than L2 ({w.algorithmic_bytes() / 1e6:.1f} MB touched per launch): steps run "
-          f"partly from L2, so this is not an HBM figure")
+          f"MB touched per launch vs {l2_bytes / 1e6:.0f} MB L2): no flush between steps" if big else
+          f"NOT larger than L2 ({w.algorithmic_bytes() / 1e6:.1f} MB touched per launch vs "
+          f"{l2_bytes / 1e6:.0f} MB L2): steps run partly from L2, so this is not an HBM figure")
     return {"workload": f"{w.name}: {w.description}; one step = {step}",
             "x_shape": list(w.shape), "partial_slice": [w.start, w.end], "r_shape": list(w.r_shape),
             "algorithmic_bytes_per_launch": w.algorithmic_bytes(), "l2": l2,
@@ -517,16 +517,17 @@ def gpu_arm(args):
                                 "no ncu summary for the current kernel sources"}
 
     e2e = e2e_measure(w, x, r1, r2, g, device, min(K, 20), binding)
+    ceiling = dense_rmw_ceiling(xd)
     out = {"metric": METRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": world,
            "steps": K, "warmup": args.warmup, "ms_per_step": round(1e3 * max_elapsed / K, 5),
            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "fp32",
            "data": "synthetic: seeded N(0,1) activations and gradients, base-10000 cos/sin table "
                    "at seeded per-batch position offsets",
-           "config": workload_config(w),
+           "config": workload_config(w, torch.cuda.get_device_properties(device).L2_cache_size),
            "frac_of_peak": round(value / world / peak, 4),
            "gelem_per_s": round(2 * w.slice_elems() * K * world / max_elapsed / 1e9, 2),
            "roofline": roofline, "e2e": e2e, "gpu_launches": nl * K * int(plan.launches),
-           "clocks": clocks,
+           "clocks": clocks, "ceiling": ceiling,
            "plan": {"vec_bytes": plan.vec_bytes, "heads_per_thread": plan.heads_per_thread,
                     "blocks": plan.blocks, "threads_per_block": plan.threads_per_block,
                     "launches_per_call": plan.launches}}
@@ -542,6 +543,26 @@ def gpu_arm(args):
         dist.destroy_process_group()
     _ = lib
     return 0
+
+
+def dense_rmw_ceiling(xd, n: int = 20) -> dict:
+    """Context for the roofline: torch's own in-place elementwise op over the
+    WHOLE x tensor (every byte read and written, fully contiguous), timed
+    back to back like the steps.  It is the practical HBM ceiling of an
+    in-place read-modify-write on this GPU; the rotation touches only the
+    slice bytes, so its achievable fraction is lower by the DRAM atoms its
+    rows cannot use."""
+    xd.mul_(1.0)
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    for _ in range(n):
+        xd.mul_(1.0)
+    b.record()
+    torch.cuda.synchronize()
+    t = a.elapsed_time(b) / 1e3 / n
+    return {"op": "torch x.mul_(1.0) over all of x (in place)", "us": round(t * 1e6, 2),
+            "GB/s": round(2 * xd.numel() * xd.element_size() / t / 1e9, 1)}
 
 
 def e2e_measure(w, x, r1, r2, g, device, steps: int, binding):
