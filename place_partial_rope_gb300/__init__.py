@@ -7,6 +7,8 @@ the library has not been built -- there is no CPU fallback.
 
 Submodules:
   binding  -- ctypes binding with the C ABI's names (loaded on first use)
+  torch_op -- the PyTorch operator, its Meta kernel and autograd
+              (inplace_partial_rotary_mul)
   synth    -- seeded synthetic inputs (no rotation arithmetic)
 """
 from __future__ import annotations
@@ -22,4 +24,7 @@ def __getattr__(name):
     if name in _BINDING_NAMES:
         from . import binding
         return getattr(binding, name)
+    if name in ("inplace_partial_rotary_mul", "InplacePartialRotaryMulFn"):
+        from . import torch_op
+        return getattr(torch_op, name)
     raise AttributeError(name)
