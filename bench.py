@@ -436,8 +436,39 @@ def breakdown(device, peak):
             entry[d] = e
         out[name] = entry
         del xd, gd, c, s
+    out["mla_decode_qk"] = qk_breakdown(device, peak, flush)
     torch.cuda.empty_cache()
     return out
+
+
+def qk_breakdown(device, peak, flush):
+    """The fused query + key MLA-decode call against two single launches
+    (query, then key), cold, per call."""
+    from place_partial_rope_gb300 import binding
+    w = synth.WORKLOADS["mla_decode_q"]
+    q, k, r1, r2 = synth.qk_inputs()
+    qd, kd = synth.to_torch(q, w.dtype).to(device), synth.to_torch(k, w.dtype).to(device)
+    c, s = synth.to_torch(r1, w.dtype).to(device), synth.to_torch(r2, w.dtype).to(device)
+    ks = synth.QK_KEY_SLICE
+    fused = binding.PreparedQK("fwd", qd, kd, c, s, (w.start, w.end), ks)
+    one_q = binding.prepare_fwd(qd, c, s, w.start, w.end)
+    one_k = binding.prepare_fwd(kd, c, s, ks[0], ks[1])
+
+    def separate():
+        one_q()
+        one_k()
+
+    for _ in range(3):
+        fused()
+        separate()
+    tf = time_launches(fused, 30, flush)
+    ts = time_launches(separate, 30, flush)
+    nbytes = synth.qk_algorithmic_bytes()
+    return {"fwd": {"fused_cold_us": round(tf * 1e6, 2), "separate_cold_us": round(ts * 1e6, 2),
+                    "fused_GB/s": round(nbytes / tf / 1e9, 1),
+                    "fused_frac": round(nbytes / tf / 1e9 / peak, 4),
+                    "what": "query (4096,1,128,192) [0,64) + key (4096,1,1,64) [0,64), bf16, one "
+                            "cos/sin row per token: one fused launch vs query then key"}}
 
 
 def gpu_arm(args):

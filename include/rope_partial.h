@@ -114,6 +114,44 @@ rope_status_t rope_partial_inplace_bwd(void* grad, const void* r1, const void* r
                                        int64_t start, int64_t end, rope_stream_t stream);
 
 /*
+ * rope_partial_inplace_fwd_qk / rope_partial_inplace_bwd_qk -- one launch
+ * that rotates a query slice and a key slice with the same cos/sin rows: the
+ * RoPE stage of MLA preprocessing, which applies the rotation to
+ * Q[..., :qRopeDim] and K[..., :kRopeDim] with cos/sin of one row per token
+ * ("ascend-transformer-boost MlaPreprocessOperation", m.xxqk.cn/news/384935,
+ * sections 3 and 4).  The result equals rope_partial_inplace_fwd on q
+ * followed by rope_partial_inplace_fwd on k (backward: _bwd on dq and dk), in
+ * one launch that reads each cos/sin row once for both.
+ *
+ *   q, k       device pointers to contiguous (B, S, Nq, Dq) and (B, S, Nk, Dk)
+ *              tensors of `dtype` (the key may have its own head count and
+ *              head dim); both are read and written.
+ *   q_start/q_end, k_start/k_end
+ *              the two slices; same rules as `start`/`end` above, and the same
+ *              length L = q_end - q_start = k_end - k_start.
+ *   r1, r2     cos and sin as above with rX_shape[2] == 1 (one row per
+ *              (batch, position), shared by every query and key head).
+ *
+ * Validation, ownership, asynchrony and status codes are those of
+ * rope_partial_inplace_fwd; a tensor whose work is empty is skipped.
+ */
+rope_status_t rope_partial_inplace_fwd_qk(void* q, void* k, const void* r1, const void* r2,
+                                          rope_dtype_t dtype, int64_t B, int64_t S,
+                                          int64_t Nq, int64_t Dq, int64_t q_start, int64_t q_end,
+                                          int64_t Nk, int64_t Dk, int64_t k_start, int64_t k_end,
+                                          const int64_t r1_shape[4], const int64_t r1_stride[4],
+                                          const int64_t r2_shape[4], const int64_t r2_stride[4],
+                                          rope_stream_t stream);
+
+rope_status_t rope_partial_inplace_bwd_qk(void* dq, void* dk, const void* r1, const void* r2,
+                                          rope_dtype_t dtype, int64_t B, int64_t S,
+                                          int64_t Nq, int64_t Dq, int64_t q_start, int64_t q_end,
+                                          int64_t Nk, int64_t Dk, int64_t k_start, int64_t k_end,
+                                          const int64_t r1_shape[4], const int64_t r1_stride[4],
+                                          const int64_t r2_shape[4], const int64_t r2_stride[4],
+                                          rope_stream_t stream);
+
+/*
  * rope_partial_inplace_fwd_host / rope_partial_inplace_bwd_host -- the same
  * operations on buffers in HOST memory, which the kernel reads and writes in
  * place across the host link (zero copy: no device buffer, no staging copy).

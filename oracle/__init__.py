@@ -134,6 +134,17 @@ def bwd(g, r1, r2, dtype, start, end, formulation=GATHER_CHAIN):
     return rope(BWD, g, r1, r2, dtype, start, end, formulation)
 
 
+def rope_qk(direction: int, q: np.ndarray, k: np.ndarray, r1: np.ndarray, r2: np.ndarray,
+            dtype: str, q_slice, k_slice, formulation: int = GATHER_CHAIN):
+    """The fused query + key call by its definition: the operation applied to
+    q and to k with the same cos/sin rows (the RoPE stage of
+    "ascend-transformer-boost MlaPreprocessOperation", section 3: rotate
+    Q[..., :qRopeDim] and K[..., :kRopeDim] with cos/sin passed in).  Pinned
+    through the single-tensor pins, since it is nothing but two of them."""
+    return (rope(direction, q, r1, r2, dtype, q_slice[0], q_slice[1], formulation),
+            rope(direction, k, r1, r2, dtype, k_slice[0], k_slice[1], formulation))
+
+
 def f32_to_bf16(a: np.ndarray) -> np.ndarray:
     a = np.ascontiguousarray(a, dtype=np.float32)
     out = np.empty(a.shape, np.uint16)

@@ -69,6 +69,11 @@ def load_library() -> ctypes.CDLL:
         fn = getattr(lib, name)
         fn.restype = ctypes.c_int
         fn.argtypes = args + [ctypes.c_void_p]
+    qk = [ctypes.c_void_p] * 4 + [ctypes.c_int] + [ctypes.c_int64] * 10 + [i64p] * 4 + [ctypes.c_void_p]
+    for name in ("rope_partial_inplace_fwd_qk", "rope_partial_inplace_bwd_qk"):
+        fn = getattr(lib, name)
+        fn.restype = ctypes.c_int
+        fn.argtypes = qk
     lib.rope_partial_plan.restype = ctypes.c_int
     lib.rope_partial_plan.argtypes = args + [ctypes.c_int32, ctypes.POINTER(RopePlan)]
     lib.rope_status_str.restype = ctypes.c_char_p
@@ -160,6 +165,53 @@ def rope_partial_inplace_bwd_host(grad: torch.Tensor, r1: torch.Tensor, r2: torc
                                   start: int, end: int, stream=None) -> None:
     """Backward on host tensors (zero copy); see rope_partial_inplace_fwd_host."""
     _call_host("rope_partial_inplace_bwd_host", grad, r1, r2, start, end, stream)
+
+
+def _qk_args(q, k, r1, r2, q_slice, k_slice, stream):
+    if q.dim() != 4 or k.dim() != 4:
+        raise RopeError(ROPE_ERR_INVALID, "q and k must be 4-D (B, S, N, D)")
+    if q.shape[:2] != k.shape[:2]:
+        raise RopeError(ROPE_ERR_INVALID, "q and k must share B and S")
+    if k.dtype != q.dtype or not k.is_contiguous() or not k.is_cuda or k.device != q.device:
+        raise RopeError(ROPE_ERR_INVALID, "k must be a contiguous CUDA tensor of q's dtype and device")
+    m = _marshal(q, r1, r2)
+    B, S, Nq, Dq = q.shape
+    Nk, Dk = k.shape[2], k.shape[3]
+    return (q.data_ptr(), k.data_ptr(), r1.data_ptr(), r2.data_ptr(), m[3], B, S, Nq, Dq,
+            int(q_slice[0]), int(q_slice[1]), Nk, Dk, int(k_slice[0]), int(k_slice[1]),
+            m[8], m[9], m[10], m[11], _stream_handle(stream, q.device))
+
+
+def rope_partial_inplace_fwd_qk(q, k, r1, r2, q_slice, k_slice, stream=None) -> None:
+    """Rotate ``q[..., q_slice]`` and ``k[..., k_slice]`` in place in one
+    launch with the same cos/sin rows (shape (B|1, S|1, 1, L))."""
+    lib = load_library()
+    with torch.cuda.device(q.device):
+        st = lib.rope_partial_inplace_fwd_qk(*_qk_args(q, k, r1, r2, q_slice, k_slice, stream))
+    _raise_for(lib, st)
+
+
+def rope_partial_inplace_bwd_qk(dq, dk, r1, r2, q_slice, k_slice, stream=None) -> None:
+    """Backward of rope_partial_inplace_fwd_qk on the two gradients, in place."""
+    lib = load_library()
+    with torch.cuda.device(dq.device):
+        st = lib.rope_partial_inplace_bwd_qk(*_qk_args(dq, dk, r1, r2, q_slice, k_slice, stream))
+    _raise_for(lib, st)
+
+
+class PreparedQK:
+    """rope_partial_inplace_{fwd,bwd}_qk with arguments marshalled once."""
+
+    def __init__(self, direction: str, q, k, r1, r2, q_slice, k_slice, stream=None):
+        self._lib = load_library()
+        self._fn = getattr(self._lib, f"rope_partial_inplace_{direction}_qk")
+        self._keep = (q, k, r1, r2)
+        self._args = _qk_args(q, k, r1, r2, q_slice, k_slice, stream)
+
+    def __call__(self) -> None:
+        st = self._fn(*self._args)
+        if st != ROPE_OK:
+            _raise_for(self._lib, st)
 
 
 class PreparedCall:

@@ -27,6 +27,14 @@ rope_status_t fail(rope_status_t st, const char* fmt, ...) {
     return st;
 }
 
+// Prefix the current message (copied first: vsnprintf must not read the
+// buffer it writes).
+rope_status_t fail_prefixed(rope_status_t st, const char* prefix) {
+    char tmp[sizeof(g_msg)];
+    snprintf(tmp, sizeof(tmp), "%s", g_msg);
+    return fail(st, "%s: %s", prefix, tmp);
+}
+
 int elem_bytes(int dtype) { return dtype == ROPE_FP32 ? 4 : 2; }
 
 struct Resolved {
@@ -126,17 +134,27 @@ int choose_heads_per_thread(int64_t N, int cap) {
     return 1;
 }
 
-rope_status_t make_plan(int dir, int dtype, const void* x, const void* r1, const void* r2,
-                        int64_t N, int64_t D, int64_t start, const Resolved& R, Plan* P) {
+// One tensor whose slice a launch rotates: the single call has one, the
+// fused query + key call two (heads of the second follow the first's).
+struct Seg {
+    void* x;
+    int64_t N, D, start;
+};
+
+rope_status_t make_plan(int dir, int dtype, const Seg* seg, int nseg, const void* r1,
+                        const void* r2, const Resolved& R, Plan* P) {
     const int e = R.e;
-    const int64_t a = start * e, Lb = R.L * e, rowb = D * e;
-    const uintptr_t px = reinterpret_cast<uintptr_t>(x), p1 = reinterpret_cast<uintptr_t>(r1),
-                    p2 = reinterpret_cast<uintptr_t>(r2);
+    const int64_t Lb = R.L * e;
+    const uintptr_t p1 = reinterpret_cast<uintptr_t>(r1), p2 = reinterpret_cast<uintptr_t>(r2);
+    int64_t N = 0;
+    for (int i = 0; i < nseg; ++i) N += seg[i].N;
     int vec = 0;
     for (int v = 16; v >= 4; v /= 2) {
         if (v < 2 * e) break;  // an access must hold whole pairs
-        bool ok = a % v == 0 && Lb % v == 0 && rowb % v == 0 && px % v == 0 && p1 % v == 0 &&
-                  p2 % v == 0;
+        bool ok = Lb % v == 0 && p1 % v == 0 && p2 % v == 0;
+        for (int i = 0; i < nseg; ++i)
+            ok = ok && (seg[i].start * e) % v == 0 && (seg[i].D * e) % v == 0 &&
+                 reinterpret_cast<uintptr_t>(seg[i].x) % v == 0;
         for (int r = 0; r < 2; ++r)
             for (int k = 0; k < 3; ++k) ok = ok && R.rb[r][k] % v == 0;
         if (ok) {
@@ -146,6 +164,7 @@ rope_status_t make_plan(int dir, int dtype, const void* x, const void* r1, const
     }
     P->dtype = dtype;
     P->dir = dir;
+    P->two = nseg == 2;
     if (vec) {
         P->path = kVector;
         P->vec = vec;
@@ -165,21 +184,28 @@ rope_status_t make_plan(int dir, int dtype, const void* x, const void* r1, const
     return ROPE_OK;
 }
 
-KernelArgs base_args(const Plan& P, void* x, const void* r1, const void* r2, int64_t N,
-                     int64_t D, int64_t start, const Resolved& R) {
+KernelArgs base_args(const Plan& P, const Seg* seg, int nseg, const void* r1, const void* r2,
+                     const Resolved& R) {
     KernelArgs k{};
-    k.x = static_cast<char*>(x) + start * R.e;
+    k.x = static_cast<char*>(seg[0].x) + seg[0].start * R.e;
+    k.row_bytes = seg[0].D * R.e;
+    k.tok_bytes = seg[0].N * seg[0].D * R.e;
+    k.N1 = static_cast<int32_t>(seg[0].N);
+    k.N = k.N1;
+    if (nseg == 2) {
+        k.x2 = static_cast<char*>(seg[1].x) + seg[1].start * R.e;
+        k.row_bytes2 = seg[1].D * R.e;
+        k.tok_bytes2 = seg[1].N * seg[1].D * R.e;
+        k.N += static_cast<int32_t>(seg[1].N);
+    }
     k.r1 = static_cast<const char*>(r1);
     k.r2 = static_cast<const char*>(r2);
-    k.row_bytes = D * R.e;
-    k.tok_bytes = N * D * R.e;
     k.r1_b = R.rb[0][0];
     k.r1_s = R.rb[0][1];
     k.r1_n = R.rb[0][2];
     k.r2_b = R.rb[1][0];
     k.r2_s = R.rb[1][1];
     k.r2_n = R.rb[1][2];
-    k.N = static_cast<int32_t>(N);
     k.H = P.H;
     k.divC = FastDiv::make(static_cast<uint32_t>(P.C));
     k.divH = FastDiv::make(static_cast<uint32_t>(P.H));
@@ -227,6 +253,38 @@ int64_t r_extent(const Resolved& R, int r, const int64_t* shape) {
     return far + R.L * R.e;
 }
 
+// Plan, size and launch every piece of a validated call.
+rope_status_t launch_all(int dir, int dtype, const Seg* seg, int nseg, const void* r1,
+                         const void* r2, const Resolved& R, int64_t B, int64_t S,
+                         rope_stream_t stream) {
+    Plan P;
+    rope_status_t st = make_plan(dir, dtype, seg, nseg, r1, r2, R, &P);
+    if (st != ROPE_OK) return st;
+
+    const char* err = nullptr;
+    int sms = 0, bps = 0;
+    if (device_sm_count(&sms, &err) != ROPE_OK) return fail(ROPE_ERR_CUDA, "%s", err);
+    if (kernel_blocks_per_sm(P, &bps, &err) != ROPE_OK) return fail(ROPE_ERR_CUDA, "%s", err);
+    if (bps < 1) bps = 1;
+
+    const KernelArgs whole = base_args(P, seg, nseg, r1, r2, R);
+    const int64_t per_tok = int64_t(P.H) * P.C;
+    return for_each_piece(B, S, per_tok, [&](const Piece& pc) -> rope_status_t {
+        KernelArgs k = whole;
+        const int64_t t0 = pc.b0 * S + pc.s0;
+        k.x += t0 * whole.tok_bytes;
+        if (k.x2) k.x2 += t0 * whole.tok_bytes2;
+        k.r1 += pc.b0 * whole.r1_b + pc.s0 * whole.r1_s;
+        k.r2 += pc.b0 * whole.r2_b + pc.s0 * whole.r2_s;
+        k.tasks = static_cast<uint32_t>(pc.count * per_tok);
+        k.divS = FastDiv::make(static_cast<uint32_t>(pc.sp));
+        const uint32_t blocks = static_cast<uint32_t>(grid_for(k.tasks, sms, bps));
+        const char* e2 = nullptr;
+        if (launch_piece(P, k, blocks, stream, &e2) != ROPE_OK) return fail(ROPE_ERR_CUDA, "%s", e2);
+        return ROPE_OK;
+    });
+}
+
 rope_status_t run(int dir, void* x, const void* r1, const void* r2, int dtype, int64_t B,
                   int64_t S, int64_t N, int64_t D, const int64_t* r1_shape,
                   const int64_t* r1_stride, const int64_t* r2_shape, const int64_t* r2_stride,
@@ -251,31 +309,37 @@ rope_status_t run(int dir, void* x, const void* r1, const void* r2, int dtype, i
         r1 = d1;
         r2 = d2;
     }
-    Plan P;
-    st = make_plan(dir, dtype, x, r1, r2, N, D, start, R, &P);
-    if (st != ROPE_OK) return st;
+    const Seg seg{x, N, D, start};
+    return launch_all(dir, dtype, &seg, 1, r1, r2, R, B, S, stream);
+}
 
-    const char* err = nullptr;
-    int sms = 0, bps = 0;
-    if (device_sm_count(&sms, &err) != ROPE_OK) return fail(ROPE_ERR_CUDA, "%s", err);
-    if (kernel_blocks_per_sm(P, &bps, &err) != ROPE_OK) return fail(ROPE_ERR_CUDA, "%s", err);
-    if (bps < 1) bps = 1;
-
-    const KernelArgs whole = base_args(P, x, r1, r2, N, D, start, R);
-    const int64_t per_tok = int64_t(P.H) * P.C;
-    return for_each_piece(B, S, per_tok, [&](const Piece& pc) -> rope_status_t {
-        KernelArgs k = whole;
-        const int64_t t0 = pc.b0 * S + pc.s0;
-        k.x += t0 * whole.tok_bytes;
-        k.r1 += pc.b0 * whole.r1_b + pc.s0 * whole.r1_s;
-        k.r2 += pc.b0 * whole.r2_b + pc.s0 * whole.r2_s;
-        k.tasks = static_cast<uint32_t>(pc.count * per_tok);
-        k.divS = FastDiv::make(static_cast<uint32_t>(pc.sp));
-        const uint32_t blocks = static_cast<uint32_t>(grid_for(k.tasks, sms, bps));
-        const char* e2 = nullptr;
-        if (launch_piece(P, k, blocks, stream, &e2) != ROPE_OK) return fail(ROPE_ERR_CUDA, "%s", e2);
-        return ROPE_OK;
-    });
+// The fused query + key call: both tensors share B, S and each token's
+// cos/sin row (r1/r2 of shape (Br, Sr, 1, L)); the slices have one length L.
+rope_status_t run_qk(int dir, void* q, void* k, const void* r1, const void* r2, int dtype,
+                     int64_t B, int64_t S, int64_t Nq, int64_t Dq, int64_t q_start, int64_t q_end,
+                     int64_t Nk, int64_t Dk, int64_t k_start, int64_t k_end,
+                     const int64_t* r1_shape, const int64_t* r1_stride, const int64_t* r2_shape,
+                     const int64_t* r2_stride, rope_stream_t stream) {
+    g_msg[0] = '\0';
+    if ((q_end - q_start) != (k_end - k_start))
+        return fail(ROPE_ERR_INVALID, "query slice length %lld and key slice length %lld differ",
+                    (long long)(q_end - q_start), (long long)(k_end - k_start));
+    if ((r1_shape && r1_shape[2] != 1) || (r2_shape && r2_shape[2] != 1))
+        return fail(ROPE_ERR_INVALID, "the fused query + key call shares one cos/sin row per "
+                    "token: r1 and r2 must have size 1 in the head dim");
+    Resolved Rq, Rk;
+    rope_status_t st = check(q, r1, r2, dtype, B, S, Nq, Dq, r1_shape, r1_stride, r2_shape,
+                             r2_stride, q_start, q_end, &Rq);
+    if (st != ROPE_OK) return fail_prefixed(st, "query");
+    st = check(k, r1, r2, dtype, B, S, Nk, Dk, r1_shape, r1_stride, r2_shape, r2_stride, k_start,
+               k_end, &Rk);
+    if (st != ROPE_OK) return fail_prefixed(st, "key");
+    Seg seg[2];
+    int nseg = 0;
+    if (!Rq.empty) seg[nseg++] = Seg{q, Nq, Dq, q_start};
+    if (!Rk.empty) seg[nseg++] = Seg{k, Nk, Dk, k_start};
+    if (nseg == 0) return ROPE_OK;
+    return launch_all(dir, dtype, seg, nseg, r1, r2, Rq.empty ? Rk : Rq, B, S, stream);
 }
 
 }  // namespace
@@ -301,6 +365,28 @@ rope_status_t rope_partial_inplace_bwd(void* grad, const void* r1, const void* r
                                        rope_stream_t stream) {
     return rope::run(rope::kBwd, grad, r1, r2, dtype, B, S, N, D, r1_shape, r1_stride, r2_shape,
                      r2_stride, start, end, stream, false);
+}
+
+rope_status_t rope_partial_inplace_fwd_qk(void* q, void* k, const void* r1, const void* r2,
+                                          rope_dtype_t dtype, int64_t B, int64_t S, int64_t Nq,
+                                          int64_t Dq, int64_t q_start, int64_t q_end, int64_t Nk,
+                                          int64_t Dk, int64_t k_start, int64_t k_end,
+                                          const int64_t r1_shape[4], const int64_t r1_stride[4],
+                                          const int64_t r2_shape[4], const int64_t r2_stride[4],
+                                          rope_stream_t stream) {
+    return rope::run_qk(rope::kFwd, q, k, r1, r2, dtype, B, S, Nq, Dq, q_start, q_end, Nk, Dk,
+                        k_start, k_end, r1_shape, r1_stride, r2_shape, r2_stride, stream);
+}
+
+rope_status_t rope_partial_inplace_bwd_qk(void* dq, void* dk, const void* r1, const void* r2,
+                                          rope_dtype_t dtype, int64_t B, int64_t S, int64_t Nq,
+                                          int64_t Dq, int64_t q_start, int64_t q_end, int64_t Nk,
+                                          int64_t Dk, int64_t k_start, int64_t k_end,
+                                          const int64_t r1_shape[4], const int64_t r1_stride[4],
+                                          const int64_t r2_shape[4], const int64_t r2_stride[4],
+                                          rope_stream_t stream) {
+    return rope::run_qk(rope::kBwd, dq, dk, r1, r2, dtype, B, S, Nq, Dq, q_start, q_end, Nk, Dk,
+                        k_start, k_end, r1_shape, r1_stride, r2_shape, r2_stride, stream);
 }
 
 rope_status_t rope_partial_inplace_fwd_host(void* x, const void* r1, const void* r2,
@@ -350,7 +436,8 @@ rope_status_t rope_partial_plan(const void* x, const void* r1, const void* r2,
                              r2_stride, start, end, &R);
     if (st != ROPE_OK || R.empty) return st;
     Plan P;
-    st = make_plan(kFwd, dtype, x, r1, r2, N, D, start, R, &P);
+    const Seg seg{const_cast<void*>(x), N, D, start};
+    st = make_plan(kFwd, dtype, &seg, 1, r1, r2, R, &P);
     if (st != ROPE_OK) return st;
     int sms = sm_count, bps = kBlocksPerSmCap;
     if (sm_count <= 0) {

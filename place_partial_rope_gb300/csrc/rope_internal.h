@@ -26,8 +26,13 @@ struct KernelArgs {
     int64_t row_bytes;         // bytes between consecutive heads of x (D * e)
     int64_t r1_b, r1_s, r1_n;  // byte strides of r1 for batch, seq, head (0: broadcast)
     int64_t r2_b, r2_s, r2_n;
+    char* x2;                  // fused query + key call: row 0 of the second tensor's
+                               // piece, plus its slice offset (nullptr otherwise)
+    int64_t tok_bytes2;        // token pitch of the second tensor
+    int64_t row_bytes2;        // head pitch of the second tensor
     uint32_t tasks;            // work items of the piece: tokens * H * C
-    int32_t N;                 // heads
+    int32_t N;                 // heads (first tensor's plus second tensor's)
+    int32_t N1;                // heads of the first tensor
     int32_t H;                 // head groups = ceil(N / U)
     FastDiv divC;              // chunks per row
     FastDiv divH;              // head groups
@@ -44,6 +49,7 @@ struct Plan {
     int H;          // head groups
     int C;          // chunks (accesses) per row slice
     bool r_head;    // cos/sin differ between heads: reloaded per head
+    bool two;       // fused query + key call (rope_partial_qk_kernel)
 };
 
 // Launch one piece on `stream` with `blocks` blocks (defined in the .cu).

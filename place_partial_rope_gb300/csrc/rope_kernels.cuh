@@ -234,16 +234,27 @@ __device__ __forceinline__ Words<W> rotate_chunk(const Words<W>& x, const Words<
 }
 
 // ------------------------------------------------------------------------
-// the kernel
+// the kernel body
 //   T      storage type            VEC    bytes per access of x
 //   SCALAR element-wise accesses   U      heads per thread
 //   DIR    kFwd / kBwd             RHEAD  cos/sin differ between heads
+//   TWO    a second tensor's heads follow the first's (the fused query + key
+//          call): head n < N1 is row n of x, head n >= N1 is row n - N1 of x2;
+//          both use the token's one cos/sin row
 // ------------------------------------------------------------------------
 
-template <typename T, int VEC, bool SCALAR, int U, int DIR, bool RHEAD>
-__global__ void __launch_bounds__(kThreads) rope_partial_kernel(const KernelArgs a) {
+template <bool TWO>
+__device__ __forceinline__ char* head_row(const KernelArgs& a, uint32_t tok, int n) {
+    if constexpr (TWO) {
+        if (n >= a.N1)
+            return a.x2 + int64_t(tok) * a.tok_bytes2 + int64_t(n - a.N1) * a.row_bytes2;
+    }
+    return a.x + int64_t(tok) * a.tok_bytes + int64_t(n) * a.row_bytes;
+}
+
+template <typename T, int VEC, bool SCALAR, int U, int DIR, bool RHEAD, bool TWO>
+__device__ __forceinline__ void rope_body(const KernelArgs& a) {
     constexpr int W = VEC / 4;
-    char* const __restrict__ xbase = a.x;
     const char* const __restrict__ r1base = a.r1;
     const char* const __restrict__ r2base = a.r2;
     const int64_t xstep = int64_t(a.H) * a.row_bytes;  // to the next head of this thread
@@ -255,10 +266,18 @@ __global__ void __launch_bounds__(kThreads) rope_partial_kernel(const KernelArgs
         a.divH.divmod(rest, tok, hg);
         a.divS.divmod(tok, b, s);
 
-        char* xp = xbase + int64_t(tok) * a.tok_bytes + int64_t(hg) * a.row_bytes +
-                   int64_t(c) * VEC;
-        const char* c_p = r1base + int64_t(b) * a.r1_b + int64_t(s) * a.r1_s + int64_t(c) * VEC;
-        const char* s_p = r2base + int64_t(b) * a.r2_b + int64_t(s) * a.r2_s + int64_t(c) * VEC;
+        const int64_t c_off = int64_t(c) * VEC;
+        char* xp[U];
+        if constexpr (TWO) {
+#pragma unroll
+            for (int i = 0; i < U; ++i) xp[i] = head_row<true>(a, tok, int(hg) + i * a.H) + c_off;
+        } else {
+            char* x0 = a.x + int64_t(tok) * a.tok_bytes + int64_t(hg) * a.row_bytes + c_off;
+#pragma unroll
+            for (int i = 0; i < U; ++i) xp[i] = x0 + i * xstep;
+        }
+        const char* c_p = r1base + int64_t(b) * a.r1_b + int64_t(s) * a.r1_s + c_off;
+        const char* s_p = r2base + int64_t(b) * a.r2_b + int64_t(s) * a.r2_s + c_off;
         if constexpr (RHEAD) {
             c_p += int64_t(hg) * a.r1_n;
             s_p += int64_t(hg) * a.r2_n;
@@ -267,7 +286,7 @@ __global__ void __launch_bounds__(kThreads) rope_partial_kernel(const KernelArgs
         Words<W> xv[U];
 #pragma unroll
         for (int i = 0; i < U; ++i)
-            if (i == 0 || int(hg) + i * a.H < a.N) xv[i] = load_x<T, W, SCALAR>(xp + i * xstep);
+            if (i == 0 || int(hg) + i * a.H < a.N) xv[i] = load_x<T, W, SCALAR>(xp[i]);
 
         Words<W> cv, sv;
         if constexpr (!RHEAD) {
@@ -281,10 +300,22 @@ __global__ void __launch_bounds__(kThreads) rope_partial_kernel(const KernelArgs
                     cv = load_r<T, W, SCALAR>(c_p + int64_t(i) * a.H * a.r1_n);
                     sv = load_r<T, W, SCALAR>(s_p + int64_t(i) * a.H * a.r2_n);
                 }
-                store_x<T, W, SCALAR>(xp + i * xstep, rotate_chunk<T, W, DIR>(xv[i], cv, sv));
+                store_x<T, W, SCALAR>(xp[i], rotate_chunk<T, W, DIR>(xv[i], cv, sv));
             }
         }
     }
+}
+
+// One tensor.
+template <typename T, int VEC, bool SCALAR, int U, int DIR, bool RHEAD>
+__global__ void __launch_bounds__(kThreads) rope_partial_kernel(const KernelArgs a) {
+    rope_body<T, VEC, SCALAR, U, DIR, RHEAD, false>(a);
+}
+
+// Query and key in one launch, sharing each token's cos/sin row.
+template <typename T, int VEC, bool SCALAR, int U, int DIR>
+__global__ void __launch_bounds__(kThreads) rope_partial_qk_kernel(const KernelArgs a) {
+    rope_body<T, VEC, SCALAR, U, DIR, false, true>(a);
 }
 
 // ------------------------------------------------------------------------
@@ -293,6 +324,9 @@ __global__ void __launch_bounds__(kThreads) rope_partial_kernel(const KernelArgs
 
 template <typename T, int VEC, bool SCALAR, int U>
 const void* pick_dir(const Plan& p) {
+    if (p.two)
+        return p.dir == kFwd ? reinterpret_cast<const void*>(&rope_partial_qk_kernel<T, VEC, SCALAR, U, kFwd>)
+                             : reinterpret_cast<const void*>(&rope_partial_qk_kernel<T, VEC, SCALAR, U, kBwd>);
     if (p.dir == kFwd)
         return p.r_head ? reinterpret_cast<const void*>(&rope_partial_kernel<T, VEC, SCALAR, U, kFwd, true>)
                         : reinterpret_cast<const void*>(&rope_partial_kernel<T, VEC, SCALAR, U, kFwd, false>);

@@ -85,6 +85,34 @@ WORKLOADS = {
 }
 
 
+# The query workload above plus its key: in MLA decoding the rope part of
+# the key is one (T, 64) row per token, rotated with the same cos/sin row as
+# the query's rope lanes [0, 64) of each 192-wide head.
+QK_KEY_SHAPE = (4096, 1, 1, 64)
+QK_KEY_SLICE = (0, 64)
+QK_KEY_SEED = 1603
+
+
+def qk_inputs(with_grad: bool = False):
+    """q, k, r1, r2 (and dq, dk) of the fused query + key MLA-decode case."""
+    w = WORKLOADS["mla_decode_q"]
+    q, r1, r2, _ = workload_inputs(w, with_grad=False)
+    k = normal(QK_KEY_SHAPE, w.dtype, QK_KEY_SEED)
+    if not with_grad:
+        return q, k, r1, r2
+    dq = normal(w.shape, w.dtype, w.seed + 500)
+    dk = normal(QK_KEY_SHAPE, w.dtype, QK_KEY_SEED + 500)
+    return q, k, r1, r2, dq, dk
+
+
+def qk_algorithmic_bytes() -> int:
+    """Slice bytes of q and k read + written, plus the unique cos/sin bytes."""
+    w = WORKLOADS["mla_decode_q"]
+    e = ELEM_BYTES[w.dtype]
+    k_elems = int(np.prod(QK_KEY_SHAPE[:3])) * (QK_KEY_SLICE[1] - QK_KEY_SLICE[0])
+    return w.algorithmic_bytes() + 2 * k_elems * e
+
+
 # --------------------------------------------------------------------------
 # storage conversions (input side only)
 # --------------------------------------------------------------------------

@@ -62,6 +62,7 @@ def test_header_symbols_are_exported(lib):
     names = set(re.findall(r"\b(rope_[a-z_]+)\s*\(", text))
     assert names == {"rope_partial_inplace_fwd", "rope_partial_inplace_bwd",
                      "rope_partial_inplace_fwd_host", "rope_partial_inplace_bwd_host",
+                     "rope_partial_inplace_fwd_qk", "rope_partial_inplace_bwd_qk",
                      "rope_status_str", "rope_last_error_message", "rope_partial_plan"}
     for n in names:
         assert hasattr(lib, n), n
@@ -232,3 +233,32 @@ int main() {
                     str(exe)], check=True)
     out = subprocess.run([str(exe)], capture_output=True, text=True)
     assert out.returncode == 0, out.stdout
+
+
+def qk_call(lib, fn="rope_partial_inplace_fwd_qk", q=BASE, k=BASE + 2**32, r1=BASE + 2**30,
+            r2=BASE + 2**31, dtype=BF16, B=4, S=1, Nq=8, Dq=192, qs=0, qe=64, Nk=1, Dk=64, ks=0,
+            ke=64, r_shape=None):
+    rs = r_shape or (B, S, 1, qe - qs)
+    rst = contig(rs)
+    return getattr(lib, fn)(q, k, r1, r2, dtype, B, S, Nq, Dq, qs, qe, Nk, Dk, ks, ke,
+                            i64(*rs), i64(*rst), i64(*rs), i64(*rst), None)
+
+
+@pytest.mark.parametrize("fn", ["rope_partial_inplace_fwd_qk", "rope_partial_inplace_bwd_qk"])
+@pytest.mark.parametrize("kwargs,status,needle", [
+    (dict(ks=0, ke=32), INVALID, "differ"),                 # slice lengths differ
+    (dict(r_shape=(4, 1, 8, 64)), INVALID, "head dim"),     # per-head cos/sin not shared
+    (dict(Dq=191), INVALID, "query"),                       # query: odd head dim
+    (dict(Dk=66, ks=4, ke=68 + 2), INVALID, "key"),         # key: slice end beyond its D
+    (dict(k=0), NULLPTR, "key"),
+    (dict(q=BASE + 1), INVALID, "query"),
+])
+def test_qk_rejected_calls(lib, fn, kwargs, status, needle):
+    st = qk_call(lib, fn, **kwargs)
+    assert st == status, (st, lib.rope_last_error_message())
+    assert needle in lib.rope_last_error_message().decode()
+
+
+def test_qk_empty_calls(lib):
+    assert qk_call(lib, qs=0, qe=0, ks=5, ke=5, q=0, k=0, r1=0, r2=0) == OK   # empty slices
+    assert qk_call(lib, B=0, q=0, k=0, r1=0, r2=0, r_shape=(1, 1, 1, 64)) == OK
