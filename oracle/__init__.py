@@ -13,6 +13,9 @@ Contents
 * ``rope_mil.py`` -- a third, array-level formulation (reshape / slice /
   negate / concat), written with numpy float32 operations.
 
+Two rotary modes: "interleave" (the page's mode, pairs (2i, 2i+1)) and
+"half" (the half-split rotate_half mode, pairs (i, i + L/2)).
+
 Sources: "CANN ops-transformer inplace_partial_rotary_mul" (formula section
 and its kernel op chain; tiling section for FP32 compute with CAST_RINT);
 "ANE实战 RoPE位置编码在MIL中的纯ANE实现" (rotate_half lowering table, backward
@@ -39,6 +42,8 @@ BF16, FP16, FP32 = 0, 1, 2
 DTYPE_CODES = {"bf16": BF16, "fp16": FP16, "fp32": FP32}
 GATHER_CHAIN, PAIR_ROTATION = 0, 1
 FWD, BWD = 0, 1
+INTERLEAVE, HALF = 1, 2
+MODE_CODES = {"interleave": INTERLEAVE, "half": HALF}
 
 _lib = None
 
@@ -56,7 +61,8 @@ def _open(path):
     lib = ctypes.CDLL(path)
     i64p = ctypes.POINTER(ctypes.c_int64)
     lib.oracle_rope.restype = ctypes.c_int
-    lib.oracle_rope.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_void_p,
+    lib.oracle_rope.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                ctypes.c_void_p,
                                 ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64,
                                 ctypes.c_int64, ctypes.c_int64, ctypes.c_int64,
                                 i64p, i64p, i64p, i64p, ctypes.c_int64, ctypes.c_int64]
@@ -99,9 +105,11 @@ def _elem_strides(arr: np.ndarray):
 
 
 def rope(direction: int, x: np.ndarray, r1: np.ndarray, r2: np.ndarray, dtype: str,
-         start: int, end: int, formulation: int = GATHER_CHAIN) -> np.ndarray:
+         start: int, end: int, formulation: int = GATHER_CHAIN,
+         mode: str = "interleave") -> np.ndarray:
     """Return a copy of ``x`` with the forward (``FWD``) or backward (``BWD``)
-    applied to lanes ``[start, end)`` of its last axis.
+    applied to lanes ``[start, end)`` of its last axis, pairing lanes
+    (2i, 2i+1) (``mode="interleave"``) or (i, i + L/2) (``mode="half"``).
 
     ``x`` is a contiguous 4-D array (B, S, N, D) holding the storage type:
     float32 for ``fp32``, uint16 bit patterns for ``bf16`` and ``fp16``.
@@ -117,7 +125,7 @@ def rope(direction: int, x: np.ndarray, r1: np.ndarray, r2: np.ndarray, dtype: s
             raise ValueError(f"oracle expects 4-D {want} arrays for {dtype}")
     out = np.ascontiguousarray(x).copy()
     B, S, N, D = out.shape
-    rc = lib.oracle_rope(direction, formulation, code,
+    rc = lib.oracle_rope(direction, formulation, MODE_CODES[mode], code,
                          out.ctypes.data, r1.ctypes.data, r2.ctypes.data, B, S, N, D,
                          _i64x4(r1.shape), _i64x4(_elem_strides(r1)),
                          _i64x4(r2.shape), _i64x4(_elem_strides(r2)), start, end)
@@ -126,12 +134,12 @@ def rope(direction: int, x: np.ndarray, r1: np.ndarray, r2: np.ndarray, dtype: s
     return out
 
 
-def fwd(x, r1, r2, dtype, start, end, formulation=GATHER_CHAIN):
-    return rope(FWD, x, r1, r2, dtype, start, end, formulation)
+def fwd(x, r1, r2, dtype, start, end, formulation=GATHER_CHAIN, mode="interleave"):
+    return rope(FWD, x, r1, r2, dtype, start, end, formulation, mode)
 
 
-def bwd(g, r1, r2, dtype, start, end, formulation=GATHER_CHAIN):
-    return rope(BWD, g, r1, r2, dtype, start, end, formulation)
+def bwd(g, r1, r2, dtype, start, end, formulation=GATHER_CHAIN, mode="interleave"):
+    return rope(BWD, g, r1, r2, dtype, start, end, formulation, mode)
 
 
 def rope_qk(direction: int, q: np.ndarray, k: np.ndarray, r1: np.ndarray, r2: np.ndarray,

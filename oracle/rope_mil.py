@@ -18,6 +18,10 @@ through the C oracle's IEEE routines (``oracle.widen`` / ``oracle.narrow``).
 The backward here is the transposed rotation on the pairs
 (dx_e = g_e c_e + g_o s_o, dx_o = g_o c_o - g_e s_e), with the same
 decomposition: reshape, slice, multiply, negate, interleave, add.
+
+Half-split mode (``mode="half"``) follows the page's prose definition of
+rotate_half ("swap the two halves of the vector and negate the front
+half"): x1, x2 = the halves, rotated = concat(-x2, x1).
 """
 from __future__ import annotations
 
@@ -35,7 +39,12 @@ def _interleave(even: np.ndarray, odd: np.ndarray) -> np.ndarray:
     return both.reshape(both.shape[:-2] + (both.shape[-2] * 2,))
 
 
-def fwd(x, r1, r2, dtype, start, end):
+def _halves(a: np.ndarray):
+    h = a.shape[-1] // 2
+    return a[..., :h], a[..., h:]
+
+
+def fwd(x, r1, r2, dtype, start, end, mode="interleave"):
     """Forward through reshape / slice / negate / concat, mul, mul, add."""
     out = np.array(x, copy=True)
     if end == start or out.size == 0:
@@ -43,16 +52,20 @@ def fwd(x, r1, r2, dtype, start, end):
     xs = widen(out[..., start:end], dtype)
     c = np.broadcast_to(widen(r1, dtype), xs.shape)
     s = np.broadcast_to(widen(r2, dtype), xs.shape)
-    q = _pairs(xs)
-    q_e, q_o = q[..., 0], q[..., 1]
-    nq = q_o * np.float32(-1.0)
-    q_rot = _interleave(nq, q_e)
+    if mode == "half":
+        x1, x2 = _halves(xs)
+        q_rot = np.concatenate([x2 * np.float32(-1.0), x1], axis=-1)
+    else:
+        q = _pairs(xs)
+        q_e, q_o = q[..., 0], q[..., 1]
+        nq = q_o * np.float32(-1.0)
+        q_rot = _interleave(nq, q_e)
     y = xs * c + q_rot * s
     out[..., start:end] = narrow(y, dtype)
     return out
 
 
-def bwd(g, r1, r2, dtype, start, end):
+def bwd(g, r1, r2, dtype, start, end, mode="interleave"):
     """Backward: the transposed rotation of the gradient, in the same style."""
     out = np.array(g, copy=True)
     if end == start or out.size == 0:
@@ -61,8 +74,12 @@ def bwd(g, r1, r2, dtype, start, end):
     c = np.broadcast_to(widen(r1, dtype), gs.shape)
     s = np.broadcast_to(widen(r2, dtype), gs.shape)
     t1 = gs * c
-    u = _pairs(gs * s)
-    u_e, u_o = u[..., 0], u[..., 1]
-    w = _interleave(u_o, u_e * np.float32(-1.0))
+    if mode == "half":
+        u1, u2 = _halves(gs * s)
+        w = np.concatenate([u2, u1 * np.float32(-1.0)], axis=-1)
+    else:
+        u = _pairs(gs * s)
+        u_e, u_o = u[..., 0], u[..., 1]
+        w = _interleave(u_o, u_e * np.float32(-1.0))
     out[..., start:end] = narrow(t1 + w, dtype)
     return out

@@ -38,6 +38,11 @@
  *     dx[2i+1] = g[2i+1]c[2i+1] - g[2i]s[2i]
  *     with the products rounded first, then one rounded add.  With a
  *     pair-duplicated table this is [P3]'s inverse rotation.
+ *   - Half-split mode (a second rotary mode): x1 and x2 are the first and
+ *     second halves of the slice and x_rotate = cat(-x2, x1) read literally,
+ *     which is [P3]'s rotate_half ("swap the two halves, negate the front
+ *     half"): lane j pairs with lane j + L/2, and the formulas above hold
+ *     with (2i, 2i+1) replaced by (j, j + L/2).
  *
  * Storage conversions (binary16 and bfloat16 to and from binary32) are
  * written out from the IEEE 754 definitions of the formats below; they call
@@ -54,6 +59,8 @@ enum { ORC_BF16 = 0, ORC_FP16 = 1, ORC_FP32 = 2 };
 enum { ORC_GATHER_CHAIN = 0, ORC_PAIR_ROTATION = 1 };
 /* direction codes */
 enum { ORC_FWD = 0, ORC_BWD = 1 };
+/* rotary modes (the interleave code is the ACLNN value 1) */
+enum { ORC_INTERLEAVE = 1, ORC_HALF = 2 };
 
 /* ------------------------------------------------------------------------ */
 /* Format conversions from the IEEE 754 definitions.                        */
@@ -215,42 +222,60 @@ static void store_elem(void* base, int64_t idx, float v, int dtype)
  *   t2[j] = -t2[j]   for even j           (InterleavedInversion, mask 0x5555...)
  *   y[j]  = t1[j] + t2[j]                 (Add)
  * Backward, the transposed chain on the gradient:
- *   t1[j] = g[j] * c[j];  u[j] = g[j] * s[j];  w[j] = u[j ^ 1];
+ *   t1[j] = g[j] * c[j];  w[j] = u[j ^ 1] with u[k] = g[k] * s[k];
  *   w[j] = -w[j] for odd j;  dx[j] = t1[j] + w[j]
+ * Half-split mode: the gather index is j + L/2 (first half) or j - L/2
+ * (second half); the forward negates the first half of the swapped
+ * product, the backward the second half.
  */
-static void row_gather_chain(int dir, float* v, const float* c, const float* s,
+static int64_t partner(int mode, int64_t j, int64_t L)
+{
+    if (mode == ORC_INTERLEAVE) return j ^ 1;
+    return j < L / 2 ? j + L / 2 : j - L / 2;
+}
+
+static int negated(int mode, int dir, int64_t j, int64_t L)
+{
+    const int first = mode == ORC_INTERLEAVE ? (j % 2 == 0) : (j < L / 2);
+    return dir == ORC_FWD ? first : !first;
+}
+
+static void row_gather_chain(int dir, int mode, float* v, const float* c, const float* s,
                              float* t1, float* t2, int64_t L)
 {
     int64_t j;
     if (dir == ORC_FWD) {
         for (j = 0; j < L; j++) t1[j] = v[j] * c[j];
-        for (j = 0; j < L; j++) t2[j] = v[j ^ 1] * s[j];
-        for (j = 0; j < L; j += 2) t2[j] = -t2[j];
+        for (j = 0; j < L; j++) t2[j] = v[partner(mode, j, L)] * s[j];
+        for (j = 0; j < L; j++) if (negated(mode, dir, j, L)) t2[j] = -t2[j];
     } else {
         for (j = 0; j < L; j++) t1[j] = v[j] * c[j];
-        for (j = 0; j < L; j++) t2[j] = v[j] * s[j];
-        for (j = 0; j < L; j += 2) { float a = t2[j]; t2[j] = t2[j + 1]; t2[j + 1] = a; }
-        for (j = 1; j < L; j += 2) t2[j] = -t2[j];
+        for (j = 0; j < L; j++) t2[j] = v[partner(mode, j, L)] * s[partner(mode, j, L)];
+        for (j = 0; j < L; j++) if (negated(mode, dir, j, L)) t2[j] = -t2[j];
     }
     for (j = 0; j < L; j++) v[j] = t1[j] + t2[j];
 }
 
 /*
- * The same result written as one 2x2 rotation per pair (spec form):
- *   fwd: y0 = x0 c0 - x1 s0 ;  y1 = x1 c1 + x0 s1
- *   bwd: d0 = g0 c0 + g1 s1 ;  d1 = g1 c1 - g0 s0
+ * The same result written as one 2x2 rotation per pair (spec form),
+ * lanes (m, n) = (2i, 2i+1) in interleave mode, (i, i + L/2) in half mode:
+ *   fwd: y_m = x_m c_m - x_n s_m ;  y_n = x_n c_n + x_m s_n
+ *   bwd: d_m = g_m c_m + g_n s_n ;  d_n = g_n c_n - g_m s_m
  */
-static void row_pair_rotation(int dir, float* v, const float* c, const float* s, int64_t L)
+static void row_pair_rotation(int dir, int mode, float* v, const float* c, const float* s,
+                              int64_t L)
 {
-    for (int64_t i = 0; i < L; i += 2) {
-        const float a = v[i], b = v[i + 1];
+    for (int64_t k = 0; k < L / 2; k++) {
+        const int64_t i = mode == ORC_INTERLEAVE ? 2 * k : k;
+        const int64_t n = mode == ORC_INTERLEAVE ? 2 * k + 1 : k + L / 2;
+        const float a = v[i], b = v[n];
         float p, q, r, t;
         if (dir == ORC_FWD) {
-            p = a * c[i];  q = b * s[i];      v[i] = p - q;
-            r = b * c[i + 1]; t = a * s[i + 1]; v[i + 1] = r + t;
+            p = a * c[i];  q = b * s[i];  v[i] = p - q;
+            r = b * c[n]; t = a * s[n]; v[n] = r + t;
         } else {
-            p = a * c[i];  q = b * s[i + 1];  v[i] = p + q;
-            r = b * c[i + 1]; t = a * s[i];   v[i + 1] = r - t;
+            p = a * c[i];  q = b * s[n];  v[i] = p + q;
+            r = b * c[n]; t = a * s[i];   v[n] = r - t;
         }
     }
 }
@@ -262,13 +287,13 @@ static void row_pair_rotation(int dir, float* v, const float* c, const float* s,
 /*
  * oracle_rope: apply the forward (dir 0) or backward (dir 1) in place to
  * the contiguous BSND tensor x (storage type `dtype`), rotating only lanes
- * [start, end) of each row.  r1 holds cos, r2 holds sin, each of shape
+ * [start, end) of each row, pairing lanes in `mode` (1 interleave, 2 half).  r1 holds cos, r2 holds sin, each of shape
  * (rX_shape[0..3]) with element strides rX_stride[0..3]; a dimension of size
  * 1 broadcasts.  formulation selects the gather chain (0) or the pair
  * rotation (1).  Returns 0, or -1 on arguments it does not accept (the
  * oracle checks only what it needs to stay in bounds).
  */
-int oracle_rope(int dir, int formulation, int dtype, void* x, const void* r1,
+int oracle_rope(int dir, int formulation, int mode, int dtype, void* x, const void* r1,
                 const void* r2, int64_t B, int64_t S, int64_t N, int64_t D,
                 const int64_t* r1_shape, const int64_t* r1_stride,
                 const int64_t* r2_shape, const int64_t* r2_stride,
@@ -276,6 +301,8 @@ int oracle_rope(int dir, int formulation, int dtype, void* x, const void* r1,
 {
     const int64_t L = end - start;
     if (B < 0 || S < 0 || N < 0 || D < 0 || start < 0 || end > D || L < 0 || (L & 1))
+        return -1;
+    if (mode != ORC_INTERLEAVE && mode != ORC_HALF)
         return -1;
     if (L == 0 || B == 0 || S == 0 || N == 0)
         return 0; /* [P1]: an empty slice or empty tensor leaves x unchanged */
@@ -310,9 +337,9 @@ int oracle_rope(int dir, int formulation, int dtype, void* x, const void* r1,
                     s[j] = load_elem(r2, o2 + j * r2_stride[3], dtype);
                 }
                 if (formulation == ORC_GATHER_CHAIN)
-                    row_gather_chain(dir, v, c, s, t1, t2, L);
+                    row_gather_chain(dir, mode, v, c, s, t1, t2, L);
                 else
-                    row_pair_rotation(dir, v, c, s, L);
+                    row_pair_rotation(dir, mode, v, c, s, L);
                 for (int64_t j = 0; j < L; j++) store_elem(x, row + j, v[j], dtype);
             }
     free(v); free(c); free(s); free(t1); free(t2);

@@ -171,13 +171,20 @@ def positions(w: Workload) -> np.ndarray:
     return np.ascontiguousarray(p)
 
 
-def rope_table(pos: np.ndarray, L: int, dtype: str, base: float = BASE):
-    """Pair-duplicated cos/sin tables of shape pos.shape + (L,)."""
+def rope_table(pos: np.ndarray, L: int, dtype: str, base: float = BASE,
+               layout: str = "interleave"):
+    """cos/sin tables of shape pos.shape + (L,): pair i's value in lanes 2i
+    and 2i+1 (``layout="interleave"``), or in lanes i and i + L/2
+    (``layout="half"``, the layout of the half-split mode)."""
     i = np.arange(L // 2, dtype=np.float64)
     inv = base ** (-(2.0 * i) / L)
     theta = pos.astype(np.float64)[..., None] * inv
-    c = np.repeat(np.cos(theta), 2, axis=-1)
-    s = np.repeat(np.sin(theta), 2, axis=-1)
+    if layout == "half":
+        c = np.concatenate([np.cos(theta)] * 2, axis=-1)
+        s = np.concatenate([np.sin(theta)] * 2, axis=-1)
+    else:
+        c = np.repeat(np.cos(theta), 2, axis=-1)
+        s = np.repeat(np.sin(theta), 2, axis=-1)
     return to_storage(c, dtype), to_storage(s, dtype)
 
 
@@ -211,7 +218,7 @@ def r_shape_for(form: str, shape, L: int):
 
 
 def case(shape, start: int, end: int, dtype: str, form: str = "BS1D", seed: int = 0,
-         table: str = "random"):
+         table: str = "random", layout: str = "interleave"):
     """A small seeded case: x, r1, r2, grad for arbitrary shapes and forms."""
     L = end - start
     rs = r_shape_for(form, shape, L)
@@ -223,5 +230,5 @@ def case(shape, start: int, end: int, dtype: str, form: str = "BS1D", seed: int 
         pos = np.broadcast_to(np.arange(rs[1], dtype=np.int64)[None, :, None] +
                               np.arange(rs[0], dtype=np.int64)[:, None, None] * 3 +
                               np.arange(rs[2], dtype=np.int64)[None, None, :] * 5, rs[:3])
-        r1, r2 = rope_table(np.ascontiguousarray(pos), L, dtype)
+        r1, r2 = rope_table(np.ascontiguousarray(pos), L, dtype, layout=layout)
     return x, r1, r2, g
