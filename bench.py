@@ -437,7 +437,32 @@ def breakdown(device, peak):
         out[name] = entry
         del xd, gd, c, s
     out["mla_decode_qk"] = qk_breakdown(device, peak, flush)
+    out["half_split"] = half_breakdown(device, peak, flush, l2)
     torch.cuda.empty_cache()
+    return out
+
+
+def half_breakdown(device, peak, flush, l2):
+    """The half-split rotary mode (pairs (i, i + L/2)) on the gqa and large
+    fp32 shapes with a half-layout cos/sin table, forward, per launch."""
+    from place_partial_rope_gb300 import binding
+    out = {}
+    for name in ("gqa", "large_unaligned"):
+        w = synth.WORKLOADS[name]
+        x = synth.normal(w.shape, w.dtype, w.seed)
+        r1, r2 = synth.rope_table(synth.positions(w), w.L, w.dtype, layout="half")
+        xd = synth.to_torch(x, w.dtype).to(device)
+        c, s = synth.to_torch(r1, w.dtype).to(device), synth.to_torch(r2, w.dtype).to(device)
+        call = binding.prepare_fwd(xd, c, s, w.start, w.end, mode="half")
+        for _ in range(3):
+            call()
+        t = time_launches(call, 30, flush)
+        tb = time_back_to_back(call, 30)
+        out[name] = {"fwd": {"cold_us": round(t * 1e6, 2),
+                             "cold_frac": round(w.algorithmic_bytes() / t / 1e9 / peak, 4),
+                             "steady_us": round(tb * 1e6, 2),
+                             "steady_frac": round(w.algorithmic_bytes() / tb / 1e9 / peak, 4)}}
+        del xd, c, s
     return out
 
 

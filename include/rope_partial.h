@@ -62,6 +62,17 @@ typedef enum {
     ROPE_FP32 = 2
 } rope_dtype_t;
 
+/* Rotary modes.  Interleave is the page's mode and numbering (the ACLNN
+   interface passes rotary_mode = 1 for interleave): lanes (2i, 2i+1) of the
+   slice form a pair.  Half-split pairs lane i with lane i + L/2, reading the
+   page's x_rotate = cat(-x2, x1) with x1, x2 the two halves of the slice,
+   which is rotate_half of "ANE实战 RoPE位置编码在MIL中的纯ANE实现" (section
+   先搞懂RoPE: swap the two halves and negate the front half). */
+typedef enum {
+    ROPE_MODE_INTERLEAVE = 1,
+    ROPE_MODE_HALF = 2
+} rope_mode_t;
+
 /* Status codes (split after the aclnn null-pointer / invalid-parameter /
    internal-error convention). */
 typedef enum {
@@ -112,6 +123,32 @@ rope_status_t rope_partial_inplace_bwd(void* grad, const void* r1, const void* r
                                        const int64_t r1_shape[4], const int64_t r1_stride[4],
                                        const int64_t r2_shape[4], const int64_t r2_stride[4],
                                        int64_t start, int64_t end, rope_stream_t stream);
+
+/*
+ * rope_partial_inplace_fwd_mode / rope_partial_inplace_bwd_mode -- the
+ * forward and backward above with an explicit rotary mode.  With
+ * ROPE_MODE_INTERLEAVE they are rope_partial_inplace_fwd / _bwd.  With
+ * ROPE_MODE_HALF, for j in [0, L/2) and m = j, n = j + L/2 (slice-relative):
+ *     y[m] = x[m] * c[m] - x[n] * s[m]        dx[m] = g[m] * c[m] + g[n] * s[n]
+ *     y[n] = x[n] * c[n] + x[m] * s[n]        dx[n] = g[n] * c[n] - g[m] * s[m]
+ * with the same rounding, validation and errors (an unknown mode returns
+ * ROPE_ERR_INVALID).
+ */
+rope_status_t rope_partial_inplace_fwd_mode(void* x, const void* r1, const void* r2,
+                                            rope_dtype_t dtype, int64_t B, int64_t S,
+                                            int64_t N, int64_t D,
+                                            const int64_t r1_shape[4], const int64_t r1_stride[4],
+                                            const int64_t r2_shape[4], const int64_t r2_stride[4],
+                                            int64_t start, int64_t end, rope_mode_t mode,
+                                            rope_stream_t stream);
+
+rope_status_t rope_partial_inplace_bwd_mode(void* grad, const void* r1, const void* r2,
+                                            rope_dtype_t dtype, int64_t B, int64_t S,
+                                            int64_t N, int64_t D,
+                                            const int64_t r1_shape[4], const int64_t r1_stride[4],
+                                            const int64_t r2_shape[4], const int64_t r2_stride[4],
+                                            int64_t start, int64_t end, rope_mode_t mode,
+                                            rope_stream_t stream);
 
 /*
  * rope_partial_inplace_fwd_qk / rope_partial_inplace_bwd_qk -- one launch
@@ -200,7 +237,8 @@ const char* rope_last_error_message(void);
  */
 typedef struct {
     int32_t path;             /* 0: no launch (empty), 1: vector kernel, 2: scalar-pair kernel */
-    int32_t vec_bytes;        /* bytes per global access of x on the vector path (16, 8 or 4)  */
+    int32_t vec_bytes;        /* bytes per global access of x (16, 8 or 4; on the scalar path  */
+                              /* a pair (interleave) or an element (half-split))                */
     int32_t heads_per_thread; /* heads one thread walks with its cos/sin kept in registers     */
     int32_t threads_per_block;
     int64_t blocks;           /* grid size                                                    */
@@ -217,6 +255,15 @@ rope_status_t rope_partial_plan(const void* x, const void* r1, const void* r2,
                                 const int64_t r2_shape[4], const int64_t r2_stride[4],
                                 int64_t start, int64_t end, int32_t sm_count,
                                 rope_plan_t* plan);
+
+/* The plan of rope_partial_inplace_fwd_mode (rope_partial_plan is this with
+   ROPE_MODE_INTERLEAVE). */
+rope_status_t rope_partial_plan_mode(const void* x, const void* r1, const void* r2,
+                                     rope_dtype_t dtype, int64_t B, int64_t S, int64_t N,
+                                     int64_t D, const int64_t r1_shape[4],
+                                     const int64_t r1_stride[4], const int64_t r2_shape[4],
+                                     const int64_t r2_stride[4], int64_t start, int64_t end,
+                                     rope_mode_t mode, int32_t sm_count, rope_plan_t* plan);
 
 #ifdef __cplusplus
 }

@@ -26,6 +26,8 @@ _LIB_PATH = os.path.join(_PKG, "librope_partial.so")
 
 ROPE_OK, ROPE_ERR_NULLPTR, ROPE_ERR_INVALID, ROPE_ERR_CUDA = 0, 1, 2, 3
 ROPE_BF16, ROPE_FP16, ROPE_FP32 = 0, 1, 2
+ROPE_MODE_INTERLEAVE, ROPE_MODE_HALF = 1, 2
+MODE_CODE = {"interleave": ROPE_MODE_INTERLEAVE, "half": ROPE_MODE_HALF}
 DTYPE_CODE = {torch.bfloat16: ROPE_BF16, torch.float16: ROPE_FP16, torch.float32: ROPE_FP32}
 
 _lib = None
@@ -69,6 +71,13 @@ def load_library() -> ctypes.CDLL:
         fn = getattr(lib, name)
         fn.restype = ctypes.c_int
         fn.argtypes = args + [ctypes.c_void_p]
+    for name in ("rope_partial_inplace_fwd_mode", "rope_partial_inplace_bwd_mode"):
+        fn = getattr(lib, name)
+        fn.restype = ctypes.c_int
+        fn.argtypes = args + [ctypes.c_int, ctypes.c_void_p]
+    lib.rope_partial_plan_mode.restype = ctypes.c_int
+    lib.rope_partial_plan_mode.argtypes = args + [ctypes.c_int, ctypes.c_int32,
+                                                  ctypes.POINTER(RopePlan)]
     qk = [ctypes.c_void_p] * 4 + [ctypes.c_int] + [ctypes.c_int64] * 10 + [i64p] * 4 + [ctypes.c_void_p]
     for name in ("rope_partial_inplace_fwd_qk", "rope_partial_inplace_bwd_qk"):
         fn = getattr(lib, name)
@@ -123,11 +132,19 @@ def _marshal(x: torch.Tensor, r1: torch.Tensor, r2: torch.Tensor, host: bool = F
             _i64x4(r1.shape), _i64x4(r1.stride()), _i64x4(r2.shape), _i64x4(r2.stride()))
 
 
-def _call(name: str, x, r1, r2, start: int, end: int, stream=None) -> None:
+def _mode_code(mode) -> int:
+    if mode in MODE_CODE:
+        return MODE_CODE[mode]
+    raise RopeError(ROPE_ERR_INVALID, f"rotary mode {mode!r} is not 'interleave' or 'half'")
+
+
+def _call(name: str, x, r1, r2, start: int, end: int, stream=None, mode=None) -> None:
     lib = load_library()
     margs = _marshal(x, r1, r2)
+    extra = () if mode is None else (_mode_code(mode),)
     with torch.cuda.device(x.device):
-        st = getattr(lib, name)(*margs, int(start), int(end), _stream_handle(stream, x.device))
+        st = getattr(lib, name)(*margs, int(start), int(end), *extra,
+                                _stream_handle(stream, x.device))
     _raise_for(lib, st)
 
 
@@ -141,6 +158,19 @@ def rope_partial_inplace_bwd(grad: torch.Tensor, r1: torch.Tensor, r2: torch.Ten
                              end: int, stream=None) -> None:
     """Overwrite ``grad[..., start:end]`` with the transposed rotation (backward)."""
     _call("rope_partial_inplace_bwd", grad, r1, r2, start, end, stream)
+
+
+def rope_partial_inplace_fwd_mode(x, r1, r2, start: int, end: int, mode: str = "interleave",
+                                  stream=None) -> None:
+    """The forward in rotary mode ``"interleave"`` or ``"half"`` (pairs
+    (i, i + L/2))."""
+    _call("rope_partial_inplace_fwd_mode", x, r1, r2, start, end, stream, mode)
+
+
+def rope_partial_inplace_bwd_mode(grad, r1, r2, start: int, end: int, mode: str = "interleave",
+                                  stream=None) -> None:
+    """The backward in rotary mode ``"interleave"`` or ``"half"``."""
+    _call("rope_partial_inplace_bwd_mode", grad, r1, r2, start, end, stream, mode)
 
 
 def _call_host(name: str, x, r1, r2, start: int, end: int, stream=None) -> None:
@@ -223,13 +253,14 @@ class PreparedCall:
     references to the tensors so their memory stays alive.
     """
 
-    def __init__(self, name: str, x, r1, r2, start: int, end: int, stream=None):
+    def __init__(self, name: str, x, r1, r2, start: int, end: int, stream=None, mode=None):
         self._lib = load_library()
         self._fn = getattr(self._lib, name)
         self._keep = (x, r1, r2)
         host = name.endswith("_host")
         dev = torch.device("cuda", torch.cuda.current_device()) if host else x.device
-        self._args = (*_marshal(x, r1, r2, host=host), int(start), int(end),
+        extra = () if mode is None else (_mode_code(mode),)
+        self._args = (*_marshal(x, r1, r2, host=host), int(start), int(end), *extra,
                       _stream_handle(stream, dev))
 
     def __call__(self) -> None:
@@ -238,14 +269,18 @@ class PreparedCall:
             _raise_for(self._lib, st)
 
 
-def prepare_fwd(x, r1, r2, start: int, end: int, stream=None) -> PreparedCall:
-    """``rope_partial_inplace_fwd`` with its arguments marshalled once."""
-    return PreparedCall("rope_partial_inplace_fwd", x, r1, r2, start, end, stream)
+def prepare_fwd(x, r1, r2, start: int, end: int, stream=None, mode=None) -> PreparedCall:
+    """``rope_partial_inplace_fwd`` (``_fwd_mode`` when a mode is given) with
+    its arguments marshalled once."""
+    name = "rope_partial_inplace_fwd" if mode is None else "rope_partial_inplace_fwd_mode"
+    return PreparedCall(name, x, r1, r2, start, end, stream, mode)
 
 
-def prepare_bwd(grad, r1, r2, start: int, end: int, stream=None) -> PreparedCall:
-    """``rope_partial_inplace_bwd`` with its arguments marshalled once."""
-    return PreparedCall("rope_partial_inplace_bwd", grad, r1, r2, start, end, stream)
+def prepare_bwd(grad, r1, r2, start: int, end: int, stream=None, mode=None) -> PreparedCall:
+    """``rope_partial_inplace_bwd`` (``_bwd_mode`` when a mode is given) with
+    its arguments marshalled once."""
+    name = "rope_partial_inplace_bwd" if mode is None else "rope_partial_inplace_bwd_mode"
+    return PreparedCall(name, grad, r1, r2, start, end, stream, mode)
 
 
 def prepare_fwd_host(x, r1, r2, start: int, end: int, stream=None) -> PreparedCall:
@@ -259,7 +294,7 @@ def prepare_bwd_host(grad, r1, r2, start: int, end: int, stream=None) -> Prepare
 
 
 def rope_partial_plan(x: torch.Tensor, r1: torch.Tensor, r2: torch.Tensor, start: int, end: int,
-                      sm_count: int = 0) -> RopePlan:
+                      sm_count: int = 0, mode: str = "interleave") -> RopePlan:
     """The launch plan the forward would use (no launch).  Works on CPU
     tensors as well when ``sm_count`` > 0, since only shapes, strides and
     pointer alignment are read."""
@@ -267,6 +302,7 @@ def rope_partial_plan(x: torch.Tensor, r1: torch.Tensor, r2: torch.Tensor, start
     plan = RopePlan()
     args = (x.data_ptr(), r1.data_ptr(), r2.data_ptr(), DTYPE_CODE[x.dtype], *x.shape,
             _i64x4(r1.shape), _i64x4(r1.stride()), _i64x4(r2.shape), _i64x4(r2.stride()))
-    st = lib.rope_partial_plan(*args, int(start), int(end), int(sm_count), ctypes.byref(plan))
+    st = lib.rope_partial_plan_mode(*args, int(start), int(end), _mode_code(mode), int(sm_count),
+                                    ctypes.byref(plan))
     _raise_for(lib, st)
     return plan

@@ -141,16 +141,19 @@ struct Seg {
     int64_t N, D, start;
 };
 
-rope_status_t make_plan(int dir, int dtype, const Seg* seg, int nseg, const void* r1,
+rope_status_t make_plan(int dir, int mode, int dtype, const Seg* seg, int nseg, const void* r1,
                         const void* r2, const Resolved& R, Plan* P) {
     const int e = R.e;
-    const int64_t Lb = R.L * e;
+    const bool half = mode == kHalf;
+    // interleave: an access holds whole pairs; half-split: an access holds
+    // lanes of the first half and its partner access lies L/2 lanes on
+    const int64_t Lb = half ? (R.L / 2) * e : R.L * e;
     const uintptr_t p1 = reinterpret_cast<uintptr_t>(r1), p2 = reinterpret_cast<uintptr_t>(r2);
     int64_t N = 0;
     for (int i = 0; i < nseg; ++i) N += seg[i].N;
     int vec = 0;
     for (int v = 16; v >= 4; v /= 2) {
-        if (v < 2 * e) break;  // an access must hold whole pairs
+        if (!half && v < 2 * e) break;  // an access must hold whole pairs
         bool ok = Lb % v == 0 && p1 % v == 0 && p2 % v == 0;
         for (int i = 0; i < nseg; ++i)
             ok = ok && (seg[i].start * e) % v == 0 && (seg[i].D * e) % v == 0 &&
@@ -165,17 +168,23 @@ rope_status_t make_plan(int dir, int dtype, const Seg* seg, int nseg, const void
     P->dtype = dtype;
     P->dir = dir;
     P->two = nseg == 2;
+    P->half = half;
     if (vec) {
         P->path = kVector;
         P->vec = vec;
         P->C = static_cast<int>(Lb / vec);
+    } else if (half) {
+        P->path = kScalarPair;  // a 16-bit slice not aligned for 4-byte accesses
+        P->vec = e;
+        P->C = static_cast<int>(R.L / 2);
     } else {
         P->path = kScalarPair;  // odd start, or a row not aligned for wide accesses
         P->vec = 2 * e;
         P->C = static_cast<int>(R.L / 2);
     }
     P->r_head = R.rb[0][2] != 0 || R.rb[1][2] != 0;
-    P->U = choose_heads_per_thread(N, P->path == kVector && vec == 16 ? 4 : 8);
+    // bytes in flight per thread: U accesses (twice that in half-split mode)
+    P->U = choose_heads_per_thread(N, (P->path == kVector && vec == 16) || half ? 4 : 8);
     const int64_t H = (N + P->U - 1) / P->U;
     if (H * P->C > int64_t(kMaxPieceTasks))
         return fail(ROPE_ERR_INVALID, "N=%lld heads with a %lld-lane slice exceed the per-token work "
@@ -207,6 +216,7 @@ KernelArgs base_args(const Plan& P, const Seg* seg, int nseg, const void* r1, co
     k.r2_s = R.rb[1][1];
     k.r2_n = R.rb[1][2];
     k.H = P.H;
+    k.half_off = P.half ? (R.L / 2) * R.e : 0;
     k.divC = FastDiv::make(static_cast<uint32_t>(P.C));
     k.divH = FastDiv::make(static_cast<uint32_t>(P.H));
     return k;
@@ -254,11 +264,11 @@ int64_t r_extent(const Resolved& R, int r, const int64_t* shape) {
 }
 
 // Plan, size and launch every piece of a validated call.
-rope_status_t launch_all(int dir, int dtype, const Seg* seg, int nseg, const void* r1,
+rope_status_t launch_all(int dir, int mode, int dtype, const Seg* seg, int nseg, const void* r1,
                          const void* r2, const Resolved& R, int64_t B, int64_t S,
                          rope_stream_t stream) {
     Plan P;
-    rope_status_t st = make_plan(dir, dtype, seg, nseg, r1, r2, R, &P);
+    rope_status_t st = make_plan(dir, mode, dtype, seg, nseg, r1, r2, R, &P);
     if (st != ROPE_OK) return st;
 
     const char* err = nullptr;
@@ -288,8 +298,11 @@ rope_status_t launch_all(int dir, int dtype, const Seg* seg, int nseg, const voi
 rope_status_t run(int dir, void* x, const void* r1, const void* r2, int dtype, int64_t B,
                   int64_t S, int64_t N, int64_t D, const int64_t* r1_shape,
                   const int64_t* r1_stride, const int64_t* r2_shape, const int64_t* r2_stride,
-                  int64_t start, int64_t end, rope_stream_t stream, bool host_buffers) {
+                  int64_t start, int64_t end, rope_stream_t stream, bool host_buffers,
+                  int mode = kInterleave) {
     g_msg[0] = '\0';
+    if (mode != kInterleave && mode != kHalf)
+        return fail(ROPE_ERR_INVALID, "rotary mode %d is not interleave (1) or half (2)", mode);
     Resolved R;
     rope_status_t st = check(x, r1, r2, dtype, B, S, N, D, r1_shape, r1_stride, r2_shape,
                              r2_stride, start, end, &R);
@@ -310,7 +323,7 @@ rope_status_t run(int dir, void* x, const void* r1, const void* r2, int dtype, i
         r2 = d2;
     }
     const Seg seg{x, N, D, start};
-    return launch_all(dir, dtype, &seg, 1, r1, r2, R, B, S, stream);
+    return launch_all(dir, mode, dtype, &seg, 1, r1, r2, R, B, S, stream);
 }
 
 // The fused query + key call: both tensors share B, S and each token's
@@ -339,7 +352,7 @@ rope_status_t run_qk(int dir, void* q, void* k, const void* r1, const void* r2, 
     if (!Rq.empty) seg[nseg++] = Seg{q, Nq, Dq, q_start};
     if (!Rk.empty) seg[nseg++] = Seg{k, Nk, Dk, k_start};
     if (nseg == 0) return ROPE_OK;
-    return launch_all(dir, dtype, seg, nseg, r1, r2, Rq.empty ? Rk : Rq, B, S, stream);
+    return launch_all(dir, kInterleave, dtype, seg, nseg, r1, r2, Rq.empty ? Rk : Rq, B, S, stream);
 }
 
 }  // namespace
@@ -365,6 +378,26 @@ rope_status_t rope_partial_inplace_bwd(void* grad, const void* r1, const void* r
                                        rope_stream_t stream) {
     return rope::run(rope::kBwd, grad, r1, r2, dtype, B, S, N, D, r1_shape, r1_stride, r2_shape,
                      r2_stride, start, end, stream, false);
+}
+
+rope_status_t rope_partial_inplace_fwd_mode(void* x, const void* r1, const void* r2,
+                                            rope_dtype_t dtype, int64_t B, int64_t S, int64_t N,
+                                            int64_t D, const int64_t r1_shape[4],
+                                            const int64_t r1_stride[4], const int64_t r2_shape[4],
+                                            const int64_t r2_stride[4], int64_t start,
+                                            int64_t end, rope_mode_t mode, rope_stream_t stream) {
+    return rope::run(rope::kFwd, x, r1, r2, dtype, B, S, N, D, r1_shape, r1_stride, r2_shape,
+                     r2_stride, start, end, stream, false, mode);
+}
+
+rope_status_t rope_partial_inplace_bwd_mode(void* grad, const void* r1, const void* r2,
+                                            rope_dtype_t dtype, int64_t B, int64_t S, int64_t N,
+                                            int64_t D, const int64_t r1_shape[4],
+                                            const int64_t r1_stride[4], const int64_t r2_shape[4],
+                                            const int64_t r2_stride[4], int64_t start,
+                                            int64_t end, rope_mode_t mode, rope_stream_t stream) {
+    return rope::run(rope::kBwd, grad, r1, r2, dtype, B, S, N, D, r1_shape, r1_stride, r2_shape,
+                     r2_stride, start, end, stream, false, mode);
 }
 
 rope_status_t rope_partial_inplace_fwd_qk(void* q, void* k, const void* r1, const void* r2,
@@ -421,23 +454,25 @@ const char* rope_status_str(rope_status_t status) {
 
 const char* rope_last_error_message(void) { return rope::g_msg; }
 
-rope_status_t rope_partial_plan(const void* x, const void* r1, const void* r2,
-                                rope_dtype_t dtype, int64_t B, int64_t S, int64_t N, int64_t D,
-                                const int64_t r1_shape[4], const int64_t r1_stride[4],
-                                const int64_t r2_shape[4], const int64_t r2_stride[4],
-                                int64_t start, int64_t end, int32_t sm_count,
-                                rope_plan_t* plan) {
+rope_status_t rope_partial_plan_mode(const void* x, const void* r1, const void* r2,
+                                     rope_dtype_t dtype, int64_t B, int64_t S, int64_t N,
+                                     int64_t D, const int64_t r1_shape[4],
+                                     const int64_t r1_stride[4], const int64_t r2_shape[4],
+                                     const int64_t r2_stride[4], int64_t start, int64_t end,
+                                     rope_mode_t mode, int32_t sm_count, rope_plan_t* plan) {
     using namespace rope;
     g_msg[0] = '\0';
     if (!plan) return fail(ROPE_ERR_NULLPTR, "plan is null");
     *plan = rope_plan_t{};
+    if (mode != kInterleave && mode != kHalf)
+        return fail(ROPE_ERR_INVALID, "rotary mode %d is not interleave (1) or half (2)", (int)mode);
     Resolved R;
     rope_status_t st = check(x, r1, r2, dtype, B, S, N, D, r1_shape, r1_stride, r2_shape,
                              r2_stride, start, end, &R);
     if (st != ROPE_OK || R.empty) return st;
     Plan P;
     const Seg seg{const_cast<void*>(x), N, D, start};
-    st = make_plan(kFwd, dtype, &seg, 1, r1, r2, R, &P);
+    st = make_plan(kFwd, mode, dtype, &seg, 1, r1, r2, R, &P);
     if (st != ROPE_OK) return st;
     int sms = sm_count, bps = kBlocksPerSmCap;
     if (sm_count <= 0) {
@@ -463,6 +498,16 @@ rope_status_t rope_partial_plan(const void* x, const void* r1, const void* r2,
     plan->r_per_head = P.r_head ? 1 : 0;
     plan->launches = launches;
     return ROPE_OK;
+}
+
+rope_status_t rope_partial_plan(const void* x, const void* r1, const void* r2,
+                                rope_dtype_t dtype, int64_t B, int64_t S, int64_t N, int64_t D,
+                                const int64_t r1_shape[4], const int64_t r1_stride[4],
+                                const int64_t r2_shape[4], const int64_t r2_stride[4],
+                                int64_t start, int64_t end, int32_t sm_count,
+                                rope_plan_t* plan) {
+    return rope_partial_plan_mode(x, r1, r2, dtype, B, S, N, D, r1_shape, r1_stride, r2_shape,
+                                  r2_stride, start, end, ROPE_MODE_INTERLEAVE, sm_count, plan);
 }
 
 }  // extern "C"

@@ -14,6 +14,7 @@ constexpr uint32_t kMaxPieceTasks = 1u << 31;  // flat work index of one launch
 
 enum Direction : int { kFwd = 0, kBwd = 1 };
 enum Path : int { kNone = 0, kVector = 1, kScalarPair = 2 };
+enum Mode : int { kInterleave = 1, kHalf = 2 };  // the ACLNN numbering: interleave = 1
 
 // What one launch covers: a contiguous range of tokens ("a piece").  The
 // kernel turns its flat work index into (token, head group, chunk) with
@@ -30,6 +31,7 @@ struct KernelArgs {
                                // piece, plus its slice offset (nullptr otherwise)
     int64_t tok_bytes2;        // token pitch of the second tensor
     int64_t row_bytes2;        // head pitch of the second tensor
+    int64_t half_off;          // half-split mode: bytes from lane j to lane j + L/2
     uint32_t tasks;            // work items of the piece: tokens * H * C
     int32_t N;                 // heads (first tensor's plus second tensor's)
     int32_t N1;                // heads of the first tensor
@@ -50,6 +52,7 @@ struct Plan {
     int C;          // chunks (accesses) per row slice
     bool r_head;    // cos/sin differ between heads: reloaded per head
     bool two;       // fused query + key call (rope_partial_qk_kernel)
+    bool half;      // half-split mode (rope_partial_half_kernel)
 };
 
 // Launch one piece on `stream` with `blocks` blocks (defined in the .cu).

@@ -181,6 +181,55 @@ __device__ __forceinline__ void st_pair_scalar(char* p, const Words<Pack<T>::kWo
     }
 }
 
+// One element through an element-sized access, in the low bits of a word
+// (the half-split mode's scalar path, where a pair's lanes are L/2 apart).
+template <typename T, bool RO>
+__device__ __forceinline__ Words<1> ld_elem_scalar(const char* p) {
+    Words<1> v;
+    if constexpr (sizeof(T) == 4) {
+        const unsigned int* q = reinterpret_cast<const unsigned int*>(p);
+        v.w[0] = RO ? __ldg(q) : q[0];
+    } else {
+        const unsigned short* q = reinterpret_cast<const unsigned short*>(p);
+        v.w[0] = RO ? __ldg(q) : q[0];
+    }
+    return v;
+}
+
+template <typename T>
+__device__ __forceinline__ void st_elem_scalar(char* p, const Words<1>& v) {
+    if constexpr (sizeof(T) == 4) *reinterpret_cast<unsigned int*>(p) = v.w[0];
+    else *reinterpret_cast<unsigned short*>(p) = static_cast<unsigned short>(v.w[0] & 0xffffu);
+}
+
+// One element held in the low bits of a word.
+template <typename T>
+struct Elem;
+
+template <>
+struct Elem<float> {
+    static __device__ __forceinline__ float get(uint32_t w) { return __uint_as_float(w); }
+    static __device__ __forceinline__ uint32_t put(float v) { return __float_as_uint(v); }
+};
+
+template <>
+struct Elem<__nv_bfloat16> {
+    static __device__ __forceinline__ float get(uint32_t w) { return __uint_as_float(w << 16); }
+    static __device__ __forceinline__ uint32_t put(float v) {
+        return __bfloat16_as_ushort(__float2bfloat16_rn(v));
+    }
+};
+
+template <>
+struct Elem<__half> {
+    static __device__ __forceinline__ float get(uint32_t w) {
+        return __half2float(__ushort_as_half(static_cast<unsigned short>(w & 0xffffu)));
+    }
+    static __device__ __forceinline__ uint32_t put(float v) {
+        return __half_as_ushort(__float2half_rn(v));
+    }
+};
+
 template <typename T, int W, bool SCALAR>
 __device__ __forceinline__ Words<W> load_x(const char* p) {
     if constexpr (SCALAR) return ld_pair_scalar<T, false>(p);
@@ -196,6 +245,26 @@ __device__ __forceinline__ Words<W> load_r(const char* p) {
 template <typename T, int W, bool SCALAR>
 __device__ __forceinline__ void store_x(char* p, const Words<W>& v) {
     if constexpr (SCALAR) st_pair_scalar<T>(p, v);
+    else st_vec<W>(p, v);
+}
+
+// Accesses of the half-split mode: vector chunks as in interleave mode, or
+// one element per access on the scalar path.
+template <typename T, int W, bool SCALAR>
+__device__ __forceinline__ Words<W> load_x_half(const char* p) {
+    if constexpr (SCALAR) return ld_elem_scalar<T, false>(p);
+    else return ld_vec<W>(p);
+}
+
+template <typename T, int W, bool SCALAR>
+__device__ __forceinline__ Words<W> load_r_half(const char* p) {
+    if constexpr (SCALAR) return ld_elem_scalar<T, true>(p);
+    else return ldg_vec<W>(p);
+}
+
+template <typename T, int W, bool SCALAR>
+__device__ __forceinline__ void store_x_half(char* p, const Words<W>& v) {
+    if constexpr (SCALAR) st_elem_scalar<T>(p, v);
     else st_vec<W>(p, v);
 }
 
@@ -233,6 +302,45 @@ __device__ __forceinline__ Words<W> rotate_chunk(const Words<W>& x, const Words<
     return y;
 }
 
+// Half-split mode: element k of chunk A (lane j) pairs with element k of
+// chunk B (lane j + L/2); cos/sin come from the same two lanes.
+template <typename T, int W, bool SCALAR, int DIR>
+__device__ __forceinline__ void rotate_half_chunks(const Words<W>& xa, const Words<W>& xb,
+                                                   const Words<W>& ca, const Words<W>& cb,
+                                                   const Words<W>& sa, const Words<W>& sb,
+                                                   Words<W>& ya, Words<W>& yb) {
+    if constexpr (SCALAR || sizeof(T) == 4) {
+        // one element per word
+#pragma unroll
+        for (int w = 0; w < W; ++w) {
+            float y0, y1;
+            rotate_pair<DIR>(Elem<T>::get(xa.w[w]), Elem<T>::get(xb.w[w]), Elem<T>::get(ca.w[w]),
+                             Elem<T>::get(cb.w[w]), Elem<T>::get(sa.w[w]), Elem<T>::get(sb.w[w]),
+                             y0, y1);
+            ya.w[w] = Elem<T>::put(y0);
+            yb.w[w] = Elem<T>::put(y1);
+        }
+    } else {
+        // two 16-bit elements per word
+        using P = Pack<T>;
+#pragma unroll
+        for (int w = 0; w < W; ++w) {
+            float a0, a1, b0, b1, c0a, c1a, c0b, c1b, s0a, s1a, s0b, s1b;
+            float ya0, ya1, yb0, yb1;
+            P::get(&xa.w[w], a0, a1);
+            P::get(&xb.w[w], b0, b1);
+            P::get(&ca.w[w], c0a, c1a);
+            P::get(&cb.w[w], c0b, c1b);
+            P::get(&sa.w[w], s0a, s1a);
+            P::get(&sb.w[w], s0b, s1b);
+            rotate_pair<DIR>(a0, b0, c0a, c0b, s0a, s0b, ya0, yb0);
+            rotate_pair<DIR>(a1, b1, c1a, c1b, s1a, s1b, ya1, yb1);
+            P::put(&ya.w[w], ya0, ya1);
+            P::put(&yb.w[w], yb0, yb1);
+        }
+    }
+}
+
 // ------------------------------------------------------------------------
 // the kernel body
 //   T      storage type            VEC    bytes per access of x
@@ -241,6 +349,8 @@ __device__ __forceinline__ Words<W> rotate_chunk(const Words<W>& x, const Words<
 //   TWO    a second tensor's heads follow the first's (the fused query + key
 //          call): head n < N1 is row n of x, head n >= N1 is row n - N1 of x2;
 //          both use the token's one cos/sin row
+//   HALF   half-split mode: the chunk covers lanes of the slice's first half
+//          and pairs with the chunk half_off bytes further on (x and cos/sin)
 // ------------------------------------------------------------------------
 
 template <bool TWO>
@@ -252,9 +362,9 @@ __device__ __forceinline__ char* head_row(const KernelArgs& a, uint32_t tok, int
     return a.x + int64_t(tok) * a.tok_bytes + int64_t(n) * a.row_bytes;
 }
 
-template <typename T, int VEC, bool SCALAR, int U, int DIR, bool RHEAD, bool TWO>
+template <typename T, int VEC, bool SCALAR, int U, int DIR, bool RHEAD, bool TWO, bool HALF>
 __device__ __forceinline__ void rope_body(const KernelArgs& a) {
-    constexpr int W = VEC / 4;
+    constexpr int W = VEC >= 4 ? VEC / 4 : 1;
     const char* const __restrict__ r1base = a.r1;
     const char* const __restrict__ r2base = a.r2;
     const int64_t xstep = int64_t(a.H) * a.row_bytes;  // to the next head of this thread
@@ -283,6 +393,41 @@ __device__ __forceinline__ void rope_body(const KernelArgs& a) {
             s_p += int64_t(hg) * a.r2_n;
         }
 
+        if constexpr (HALF) {
+            const int64_t ho = a.half_off;
+            Words<W> xa[U], xb[U];
+#pragma unroll
+            for (int i = 0; i < U; ++i)
+                if (i == 0 || int(hg) + i * a.H < a.N) {
+                    xa[i] = load_x_half<T, W, SCALAR>(xp[i]);
+                    xb[i] = load_x_half<T, W, SCALAR>(xp[i] + ho);
+                }
+            Words<W> ca, cb, sa, sb;
+            if constexpr (!RHEAD) {
+                ca = load_r_half<T, W, SCALAR>(c_p);
+                cb = load_r_half<T, W, SCALAR>(c_p + ho);
+                sa = load_r_half<T, W, SCALAR>(s_p);
+                sb = load_r_half<T, W, SCALAR>(s_p + ho);
+            }
+#pragma unroll
+            for (int i = 0; i < U; ++i) {
+                if (i == 0 || int(hg) + i * a.H < a.N) {
+                    if constexpr (RHEAD) {
+                        const int64_t o1 = int64_t(i) * a.H * a.r1_n, o2 = int64_t(i) * a.H * a.r2_n;
+                        ca = load_r_half<T, W, SCALAR>(c_p + o1);
+                        cb = load_r_half<T, W, SCALAR>(c_p + o1 + ho);
+                        sa = load_r_half<T, W, SCALAR>(s_p + o2);
+                        sb = load_r_half<T, W, SCALAR>(s_p + o2 + ho);
+                    }
+                    Words<W> ya, yb;
+                    rotate_half_chunks<T, W, SCALAR, DIR>(xa[i], xb[i], ca, cb, sa, sb, ya, yb);
+                    store_x_half<T, W, SCALAR>(xp[i], ya);
+                    store_x_half<T, W, SCALAR>(xp[i] + ho, yb);
+                }
+            }
+            continue;
+        }
+
         Words<W> xv[U];
 #pragma unroll
         for (int i = 0; i < U; ++i)
@@ -309,55 +454,96 @@ __device__ __forceinline__ void rope_body(const KernelArgs& a) {
 // One tensor.
 template <typename T, int VEC, bool SCALAR, int U, int DIR, bool RHEAD>
 __global__ void __launch_bounds__(kThreads) rope_partial_kernel(const KernelArgs a) {
-    rope_body<T, VEC, SCALAR, U, DIR, RHEAD, false>(a);
+    rope_body<T, VEC, SCALAR, U, DIR, RHEAD, false, false>(a);
 }
 
 // Query and key in one launch, sharing each token's cos/sin row.
 template <typename T, int VEC, bool SCALAR, int U, int DIR>
 __global__ void __launch_bounds__(kThreads) rope_partial_qk_kernel(const KernelArgs a) {
-    rope_body<T, VEC, SCALAR, U, DIR, false, true>(a);
+    rope_body<T, VEC, SCALAR, U, DIR, false, true, false>(a);
+}
+
+// One tensor, half-split mode (pairs (j, j + L/2)).
+template <typename T, int VEC, bool SCALAR, int U, int DIR, bool RHEAD>
+__global__ void __launch_bounds__(kThreads) rope_partial_half_kernel(const KernelArgs a) {
+    rope_body<T, VEC, SCALAR, U, DIR, RHEAD, false, true>(a);
 }
 
 // ------------------------------------------------------------------------
 // kernel selection for one storage type (instantiated in one .cu per type)
 // ------------------------------------------------------------------------
 
-template <typename T, int VEC, bool SCALAR, int U>
+enum Kind { kSingle, kQK, kHalfSplit };
+
+template <typename T, int VEC, bool SCALAR, int U, Kind K>
 const void* pick_dir(const Plan& p) {
-    if (p.two)
-        return p.dir == kFwd ? reinterpret_cast<const void*>(&rope_partial_qk_kernel<T, VEC, SCALAR, U, kFwd>)
-                             : reinterpret_cast<const void*>(&rope_partial_qk_kernel<T, VEC, SCALAR, U, kBwd>);
-    if (p.dir == kFwd)
-        return p.r_head ? reinterpret_cast<const void*>(&rope_partial_kernel<T, VEC, SCALAR, U, kFwd, true>)
-                        : reinterpret_cast<const void*>(&rope_partial_kernel<T, VEC, SCALAR, U, kFwd, false>);
-    return p.r_head ? reinterpret_cast<const void*>(&rope_partial_kernel<T, VEC, SCALAR, U, kBwd, true>)
-                    : reinterpret_cast<const void*>(&rope_partial_kernel<T, VEC, SCALAR, U, kBwd, false>);
+    const bool f = p.dir == kFwd;
+    if constexpr (K == kQK) {
+        return f ? reinterpret_cast<const void*>(&rope_partial_qk_kernel<T, VEC, SCALAR, U, kFwd>)
+                 : reinterpret_cast<const void*>(&rope_partial_qk_kernel<T, VEC, SCALAR, U, kBwd>);
+    } else if constexpr (K == kHalfSplit) {
+        if (f)
+            return p.r_head ? reinterpret_cast<const void*>(&rope_partial_half_kernel<T, VEC, SCALAR, U, kFwd, true>)
+                            : reinterpret_cast<const void*>(&rope_partial_half_kernel<T, VEC, SCALAR, U, kFwd, false>);
+        return p.r_head ? reinterpret_cast<const void*>(&rope_partial_half_kernel<T, VEC, SCALAR, U, kBwd, true>)
+                        : reinterpret_cast<const void*>(&rope_partial_half_kernel<T, VEC, SCALAR, U, kBwd, false>);
+    } else {
+        if (f)
+            return p.r_head ? reinterpret_cast<const void*>(&rope_partial_kernel<T, VEC, SCALAR, U, kFwd, true>)
+                            : reinterpret_cast<const void*>(&rope_partial_kernel<T, VEC, SCALAR, U, kFwd, false>);
+        return p.r_head ? reinterpret_cast<const void*>(&rope_partial_kernel<T, VEC, SCALAR, U, kBwd, true>)
+                        : reinterpret_cast<const void*>(&rope_partial_kernel<T, VEC, SCALAR, U, kBwd, false>);
+    }
 }
 
-template <typename T, int VEC, bool SCALAR>
+template <typename T, int VEC, bool SCALAR, Kind K>
 const void* pick_heads(const Plan& p) {
     switch (p.U) {
-        case 1: return pick_dir<T, VEC, SCALAR, 1>(p);
-        case 2: return pick_dir<T, VEC, SCALAR, 2>(p);
-        case 4: return pick_dir<T, VEC, SCALAR, 4>(p);
+        case 1: return pick_dir<T, VEC, SCALAR, 1, K>(p);
+        case 2: return pick_dir<T, VEC, SCALAR, 2, K>(p);
+        case 4: return pick_dir<T, VEC, SCALAR, 4, K>(p);
         case 8:
-            if constexpr (VEC < 16) return pick_dir<T, VEC, SCALAR, 8>(p);
+            if constexpr (VEC < 16) return pick_dir<T, VEC, SCALAR, 8, K>(p);
             else return nullptr;
+        default: return nullptr;
+    }
+}
+
+// Interleave mode (single tensor or query + key): 16/8/4-byte chunks of
+// whole pairs, or a pair through element accesses.
+template <typename T, Kind K>
+const void* pick_interleave(const Plan& p) {
+    if (p.path == kScalarPair) return pick_heads<T, 2 * sizeof(T), true, K>(p);
+    switch (p.vec) {
+        case 16: return pick_heads<T, 16, false, K>(p);
+        case 8: return pick_heads<T, 8, false, K>(p);
+        case 4:
+            if constexpr (sizeof(T) == 2) return pick_heads<T, 4, false, K>(p);
+            else return nullptr;
+        default: return nullptr;
+    }
+}
+
+// Half-split mode: 16/8/4-byte chunks, or single 16-bit elements.
+template <typename T>
+const void* pick_half(const Plan& p) {
+    if (p.path == kScalarPair) {
+        if constexpr (sizeof(T) == 2) return pick_heads<T, 2, true, kHalfSplit>(p);
+        else return nullptr;  // an fp32 element is a 4-byte chunk
+    }
+    switch (p.vec) {
+        case 16: return pick_heads<T, 16, false, kHalfSplit>(p);
+        case 8: return pick_heads<T, 8, false, kHalfSplit>(p);
+        case 4: return pick_heads<T, 4, false, kHalfSplit>(p);
         default: return nullptr;
     }
 }
 
 template <typename T>
 const void* pick_kernel(const Plan& p) {
-    if (p.path == kScalarPair) return pick_heads<T, 2 * sizeof(T), true>(p);
-    switch (p.vec) {
-        case 16: return pick_heads<T, 16, false>(p);
-        case 8: return pick_heads<T, 8, false>(p);
-        case 4:
-            if constexpr (sizeof(T) == 2) return pick_heads<T, 4, false>(p);
-            else return nullptr;
-        default: return nullptr;
-    }
+    if (p.half) return pick_half<T>(p);
+    if (p.two) return pick_interleave<T, kQK>(p);
+    return pick_interleave<T, kSingle>(p);
 }
 
 // defined in rope_kernels_{bf16,fp16,fp32}.cu

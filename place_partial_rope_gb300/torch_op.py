@@ -16,6 +16,8 @@ inplace_partial_rotary_mul" (sections å‡½æ•°åŽŸåž‹ä¸Žå‚æ•°è¯´æ˜Ž, è‡ªåŠ¨å¾®åˆ†è
   only, for fake tensors and tracing).  There is no CPU kernel: CPU tensors
   fail in the dispatcher.
 * ``partial_slice=None`` means [0, 0], an empty slice (a no-op).
+* ``rotary_mode``: "interleave" (the page's only mode: pairs (2i, 2i+1)) or
+  "half" (half-split rotate_half: pairs (i, i + L/2)); anything else raises.
 * When ``x.requires_grad`` and grad mode is on, the call goes through
   ``InplacePartialRotaryMulFn``: the forward marks x dirty and saves r1 and
   r2; the backward applies the transposed rotation to the incoming
@@ -36,7 +38,7 @@ from . import binding
 NAMESPACE = "place_partial_rope"
 _FWD = "inplace_partial_rotary_mul"
 _BWD = "inplace_partial_rotary_mul_backward"
-_MODES = ("interleave",)
+_MODES = ("interleave", "half")
 
 _lib = None
 
@@ -46,8 +48,8 @@ def _check(x: torch.Tensor, rotary_mode: str, partial_slice: Sequence[int]) -> N
     if x.dim() != 4:
         raise ValueError(f"inplace_partial_rotary_mul: x must be 4-D (B, S, N, D), got {x.dim()}-D")
     if rotary_mode not in _MODES:
-        raise ValueError(f"inplace_partial_rotary_mul: rotary_mode must be 'interleave', "
-                         f"got {rotary_mode!r}")
+        raise ValueError(f"inplace_partial_rotary_mul: rotary_mode must be 'interleave' or "
+                         f"'half', got {rotary_mode!r}")
     if len(partial_slice) != 2:
         raise ValueError(f"inplace_partial_rotary_mul: partial_slice must hold 2 integers, "
                          f"got {len(partial_slice)}")
@@ -55,12 +57,14 @@ def _check(x: torch.Tensor, rotary_mode: str, partial_slice: Sequence[int]) -> N
 
 def _cuda_fwd(x, r1, r2, rotary_mode="interleave", partial_slice=(0, 0)):
     _check(x, rotary_mode, partial_slice)
-    binding.rope_partial_inplace_fwd(x, r1, r2, int(partial_slice[0]), int(partial_slice[1]))
+    binding.rope_partial_inplace_fwd_mode(x, r1, r2, int(partial_slice[0]), int(partial_slice[1]),
+                                          rotary_mode)
 
 
 def _cuda_bwd(grad, r1, r2, rotary_mode="interleave", partial_slice=(0, 0)):
     _check(grad, rotary_mode, partial_slice)
-    binding.rope_partial_inplace_bwd(grad, r1, r2, int(partial_slice[0]), int(partial_slice[1]))
+    binding.rope_partial_inplace_bwd_mode(grad, r1, r2, int(partial_slice[0]),
+                                          int(partial_slice[1]), rotary_mode)
 
 
 def _meta(x, r1, r2, rotary_mode="interleave", partial_slice=(0, 0)):

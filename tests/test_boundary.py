@@ -63,6 +63,8 @@ def test_header_symbols_are_exported(lib):
     assert names == {"rope_partial_inplace_fwd", "rope_partial_inplace_bwd",
                      "rope_partial_inplace_fwd_host", "rope_partial_inplace_bwd_host",
                      "rope_partial_inplace_fwd_qk", "rope_partial_inplace_bwd_qk",
+                     "rope_partial_inplace_fwd_mode", "rope_partial_inplace_bwd_mode",
+                     "rope_partial_plan_mode",
                      "rope_status_str", "rope_last_error_message", "rope_partial_plan"}
     for n in names:
         assert hasattr(lib, n), n
@@ -262,3 +264,46 @@ def test_qk_rejected_calls(lib, fn, kwargs, status, needle):
 def test_qk_empty_calls(lib):
     assert qk_call(lib, qs=0, qe=0, ks=5, ke=5, q=0, k=0, r1=0, r2=0) == OK   # empty slices
     assert qk_call(lib, B=0, q=0, k=0, r1=0, r2=0, r_shape=(1, 1, 1, 64)) == OK
+
+
+def plan_mode(lib, mode, x=BASE, r1=BASE + 2**30, r2=BASE + 2**31, dtype=FP16, shape=(2, 4, 3, 16),
+              start=0, end=8, r_shape=None):
+    B, S, N, D = shape
+    rs = r_shape or (1, S, 1, end - start)
+    rst = contig(rs)
+    p = binding.RopePlan()
+    st = lib.rope_partial_plan_mode(x, r1, r2, dtype, B, S, N, D, i64(*rs), i64(*rst), i64(*rs),
+                                    i64(*rst), start, end, mode, 152, ctypes.byref(p))
+    return st, p
+
+
+def test_half_split_plans(lib):
+    HALF = 2
+    # gqa-like fp16: each half of the 64-lane slice is 64 bytes -> 16-byte chunks
+    st, p = plan_mode(lib, HALF, shape=(32, 2048, 16, 128), start=0, end=64, r_shape=(1, 2048, 1, 64))
+    assert st == OK and (p.path, p.vec_bytes, p.chunks_per_row, p.heads_per_thread) == (1, 16, 4, 4)
+    # fp32 slice at byte 136: each half 128 bytes, chunks of 8 bytes (one pair of lanes per half)
+    st, p = plan_mode(lib, HALF, dtype=FP32, shape=(4, 8192, 32, 128), start=34, end=98,
+                      r_shape=(4, 8192, 1, 64))
+    assert st == OK and (p.path, p.vec_bytes, p.chunks_per_row) == (1, 8, 16)
+    # fp16 odd start: single elements
+    st, p = plan_mode(lib, HALF, start=1, end=9)
+    assert st == OK and (p.path, p.vec_bytes, p.chunks_per_row) == (2, 2, 4)
+    # fp32 odd start: a 4-byte chunk is one element
+    st, p = plan_mode(lib, HALF, dtype=FP32, start=1, end=9)
+    assert st == OK and (p.path, p.vec_bytes, p.chunks_per_row) == (1, 4, 4)
+    # half of L = 2 lanes of fp16 is 4 bytes
+    st, p = plan_mode(lib, HALF, start=0, end=4)
+    assert st == OK and (p.path, p.vec_bytes, p.chunks_per_row) == (1, 4, 1)
+
+
+@pytest.mark.parametrize("mode", [0, 3, -1])
+def test_unknown_mode_rejected(lib, mode):
+    st, _ = plan_mode(lib, mode)
+    assert st == INVALID and "mode" in lib.rope_last_error_message().decode()
+    B, S, N, D = 2, 4, 3, 16
+    rs = (1, S, 1, 8)
+    for fn in (lib.rope_partial_inplace_fwd_mode, lib.rope_partial_inplace_bwd_mode):
+        st = fn(BASE, BASE + 2**30, BASE + 2**31, FP16, B, S, N, D, i64(*rs), i64(*contig(rs)),
+                i64(*rs), i64(*contig(rs)), 0, 8, mode, None)
+        assert st == INVALID

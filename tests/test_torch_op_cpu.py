@@ -39,7 +39,7 @@ def test_meta_kernel_accepts_valid_calls():
 @pytest.mark.parametrize("x,mode,ps,needle", [
     (meta(2, 4, 16), "interleave", [0, 8], "4-D"),
     (meta(1, 2, 4, 3, 16), "interleave", [0, 8], "4-D"),
-    (meta(2, 4, 3, 16), "half", [0, 8], "interleave"),
+    (meta(2, 4, 3, 16), "neox", [0, 8], "interleave"),
     (meta(2, 4, 3, 16), "interleave", [0, 8, 2], "2 integers"),
     (meta(2, 4, 3, 16), "interleave", [4], "2 integers"),
 ])
