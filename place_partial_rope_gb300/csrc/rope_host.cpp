@@ -125,6 +125,24 @@ rope_status_t check(const void* x, const void* r1, const void* r2, int dtype, in
 // ceil(N / U) * U head slots leave at most a quarter idle.  An idle slot
 // costs issue slots, not memory traffic, so a larger U (more accesses in
 // flight, cos/sin reused more) wins over a perfect fit.
+//
+// The cap comes from back-to-back timings on GB300 of every access kind
+// (U = 1, 2, 4, 8 on the workloads' shapes).  fp32 rows want few heads per
+// thread: 16-byte chunks ran 87 us at U = 1 against 92 us at U = 4, and
+// 8-byte chunks 105 us at U = 2 against 115 us at U = 8 (half-split: U = 1,
+// 104 us against 112 us).  16-bit rows want 4: 16-byte chunks are flat from
+// U = 2 to 8 on 256-byte rows and best at 4 on 384-byte rows; 4-byte chunks
+// ran 62 us at U = 4 against 64 us at 8; the element path is best at 8.
+int heads_cap(bool half, int e, int vec, int path) {
+    if (path == kScalarPair) return half ? 4 : 8;
+    if (e == 4) {
+        if (half) return 1;
+        return vec == 16 ? 1 : 2;
+    }
+    if (half) return vec == 16 ? 4 : 2;
+    return vec == 8 ? 2 : 4;
+}
+
 int choose_heads_per_thread(int64_t N, int cap) {
     for (int u = cap; u > 1; u /= 2) {
         if (u > N) continue;
@@ -183,8 +201,7 @@ rope_status_t make_plan(int dir, int mode, int dtype, const Seg* seg, int nseg, 
         P->C = static_cast<int>(R.L / 2);
     }
     P->r_head = R.rb[0][2] != 0 || R.rb[1][2] != 0;
-    // bytes in flight per thread: U accesses (twice that in half-split mode)
-    P->U = choose_heads_per_thread(N, (P->path == kVector && vec == 16) || half ? 4 : 8);
+    P->U = choose_heads_per_thread(N, heads_cap(half, e, P->vec, P->path));
     const int64_t H = (N + P->U - 1) / P->U;
     if (H * P->C > int64_t(kMaxPieceTasks))
         return fail(ROPE_ERR_INVALID, "N=%lld heads with a %lld-lane slice exceed the per-token work "

@@ -160,10 +160,10 @@ def test_plans_of_the_named_workloads(lib):
     assert (p.path, p.vec_bytes, p.chunks_per_row, p.heads_per_thread) == (1, 16, 8, 4)
     # large fp32 with the slice at byte 136: 8-byte accesses hold whole pairs
     p = plan(lib, dtype=FP32, shape=(4, 8192, 32, 128), start=34, end=98, r_shape=(4, 8192, 1, 64))
-    assert (p.path, p.vec_bytes, p.chunks_per_row, p.heads_per_thread) == (1, 8, 32, 8)
+    assert (p.path, p.vec_bytes, p.chunks_per_row, p.heads_per_thread) == (1, 8, 32, 2)
     # tiny fp32 and the small-model bf16 full-row slice
     p = plan(lib, dtype=FP32, shape=(1, 16, 2, 64), start=0, end=32, r_shape=(1, 16, 1, 32))
-    assert (p.path, p.vec_bytes, p.heads_per_thread, p.blocks) == (1, 16, 2, 1)
+    assert (p.path, p.vec_bytes, p.heads_per_thread, p.blocks) == (1, 16, 1, 1)
     p = plan(lib, dtype=BF16, shape=(16, 256, 12, 64), start=0, end=64, r_shape=(1, 256, 1, 64))
     assert (p.path, p.vec_bytes, p.heads_per_thread) == (1, 16, 4)
 
@@ -183,8 +183,11 @@ def test_path_choice(lib):
 
 
 @pytest.mark.parametrize("N,vec,U", [(1, 16, 1), (2, 16, 2), (3, 16, 2), (5, 16, 2), (7, 16, 4),
-                                     (12, 16, 4), (16, 16, 4), (12, 8, 8), (32, 8, 8), (6, 8, 4)])
+                                     (12, 16, 4), (16, 16, 4), (12, 8, 2), (32, 8, 2), (6, 8, 2),
+                                     (5, 8, 2)])
 def test_heads_per_thread(lib, N, vec, U):
+    """16-bit rows: up to 4 heads per thread for 16-byte chunks, 2 for 8-byte
+    chunks, never more than a quarter of the head slots idle."""
     start = 0 if vec == 16 else 4  # 8-byte slice offset forces 8-byte accesses for fp16
     p = plan(lib, shape=(1, 2, N, 24), start=start, end=start + 8, r_shape=(1, 2, 1, 8))
     assert p.vec_bytes == vec and p.heads_per_thread == U
