@@ -35,7 +35,8 @@ struct KernelArgs {
     uint32_t tasks;            // work items of the piece: tokens * H * C
     int32_t N;                 // heads (first tensor's plus second tensor's)
     int32_t N1;                // heads of the first tensor
-    int32_t H;                 // head groups = ceil(N / U)
+    int32_t H;                 // head groups = ceil(N / U); group hg holds heads
+                               // hg*U .. hg*U + U - 1
     FastDiv divC;              // chunks per row
     FastDiv divH;              // head groups
     FastDiv divS;              // tokens per batch inside the piece
@@ -53,6 +54,8 @@ struct Plan {
     bool r_head;    // cos/sin differ between heads: reloaded per head
     bool two;       // fused query + key call (rope_partial_qk_kernel)
     bool half;      // half-split mode (rope_partial_half_kernel)
+    bool full_grid; // one block per 256 work items instead of a resident,
+                    // grid-striding grid
 };
 
 // Launch one piece on `stream` with `blocks` blocks (defined in the .cu).

@@ -19,14 +19,16 @@
 //     so the pair swap happens inside a thread's registers (no shuffles);
 //     rows whose slice is not aligned for that fall back to a scalar path
 //     with one access per element ("scalar pair");
-//   * a thread keeps the chunk's cos/sin in registers and walks U heads of
-//     the same token (heads hg, hg+H, ..., H = ceil(N/U)), issuing all U
-//     loads of x before any arithmetic, so U accesses per thread are in
-//     flight and the cos/sin bytes are read once per U heads;
+//   * a thread keeps the chunk's cos/sin in registers and walks U
+//     consecutive heads of the same token (heads hg*U .. hg*U + U - 1),
+//     issuing all U loads of x before any arithmetic, so U accesses per
+//     thread are in flight and the cos/sin bytes are read once per U heads;
 //   * consecutive threads take consecutive chunks of a row, so a warp reads
 //     whole 32-byte sectors of each row's slice;
-//   * the grid is sized to the resident blocks of all SMs and strides over
-//     the flat work index (three multiply-high divisions per item).
+//   * the flat work index is split by three multiply-high divisions per
+//     item; the grid either covers it once (16-bit interleave) or is sized to
+//     the resident blocks of all SMs and strides over it (the host picks the
+//     faster, measured per access kind).
 // Only slice bytes are read or written; every other byte of x is untouched.
 #pragma once
 #include <cuda_bf16.h>
@@ -367,7 +369,6 @@ __device__ __forceinline__ void rope_body(const KernelArgs& a) {
     constexpr int W = VEC >= 4 ? VEC / 4 : 1;
     const char* const __restrict__ r1base = a.r1;
     const char* const __restrict__ r2base = a.r2;
-    const int64_t xstep = int64_t(a.H) * a.row_bytes;  // to the next head of this thread
     const uint64_t stride = uint64_t(gridDim.x) * kThreads;
 
     for (uint64_t t = uint64_t(blockIdx.x) * kThreads + threadIdx.x; t < a.tasks; t += stride) {
@@ -376,21 +377,23 @@ __device__ __forceinline__ void rope_body(const KernelArgs& a) {
         a.divH.divmod(rest, tok, hg);
         a.divS.divmod(tok, b, s);
 
+        // this thread's heads are n0 .. n0 + U - 1 (consecutive rows)
+        const int n0 = int(hg) * U;
         const int64_t c_off = int64_t(c) * VEC;
         char* xp[U];
         if constexpr (TWO) {
 #pragma unroll
-            for (int i = 0; i < U; ++i) xp[i] = head_row<true>(a, tok, int(hg) + i * a.H) + c_off;
+            for (int i = 0; i < U; ++i) xp[i] = head_row<true>(a, tok, n0 + i) + c_off;
         } else {
-            char* x0 = a.x + int64_t(tok) * a.tok_bytes + int64_t(hg) * a.row_bytes + c_off;
+            char* x0 = a.x + int64_t(tok) * a.tok_bytes + int64_t(n0) * a.row_bytes + c_off;
 #pragma unroll
-            for (int i = 0; i < U; ++i) xp[i] = x0 + i * xstep;
+            for (int i = 0; i < U; ++i) xp[i] = x0 + i * a.row_bytes;
         }
         const char* c_p = r1base + int64_t(b) * a.r1_b + int64_t(s) * a.r1_s + c_off;
         const char* s_p = r2base + int64_t(b) * a.r2_b + int64_t(s) * a.r2_s + c_off;
         if constexpr (RHEAD) {
-            c_p += int64_t(hg) * a.r1_n;
-            s_p += int64_t(hg) * a.r2_n;
+            c_p += int64_t(n0) * a.r1_n;
+            s_p += int64_t(n0) * a.r2_n;
         }
 
         if constexpr (HALF) {
@@ -398,7 +401,7 @@ __device__ __forceinline__ void rope_body(const KernelArgs& a) {
             Words<W> xa[U], xb[U];
 #pragma unroll
             for (int i = 0; i < U; ++i)
-                if (i == 0 || int(hg) + i * a.H < a.N) {
+                if (i == 0 || n0 + i < a.N) {
                     xa[i] = load_x_half<T, W, SCALAR>(xp[i]);
                     xb[i] = load_x_half<T, W, SCALAR>(xp[i] + ho);
                 }
@@ -411,9 +414,9 @@ __device__ __forceinline__ void rope_body(const KernelArgs& a) {
             }
 #pragma unroll
             for (int i = 0; i < U; ++i) {
-                if (i == 0 || int(hg) + i * a.H < a.N) {
+                if (i == 0 || n0 + i < a.N) {
                     if constexpr (RHEAD) {
-                        const int64_t o1 = int64_t(i) * a.H * a.r1_n, o2 = int64_t(i) * a.H * a.r2_n;
+                        const int64_t o1 = int64_t(i) * a.r1_n, o2 = int64_t(i) * a.r2_n;
                         ca = load_r_half<T, W, SCALAR>(c_p + o1);
                         cb = load_r_half<T, W, SCALAR>(c_p + o1 + ho);
                         sa = load_r_half<T, W, SCALAR>(s_p + o2);
@@ -431,7 +434,7 @@ __device__ __forceinline__ void rope_body(const KernelArgs& a) {
         Words<W> xv[U];
 #pragma unroll
         for (int i = 0; i < U; ++i)
-            if (i == 0 || int(hg) + i * a.H < a.N) xv[i] = load_x<T, W, SCALAR>(xp[i]);
+            if (i == 0 || n0 + i < a.N) xv[i] = load_x<T, W, SCALAR>(xp[i]);
 
         Words<W> cv, sv;
         if constexpr (!RHEAD) {
@@ -440,10 +443,10 @@ __device__ __forceinline__ void rope_body(const KernelArgs& a) {
         }
 #pragma unroll
         for (int i = 0; i < U; ++i) {
-            if (i == 0 || int(hg) + i * a.H < a.N) {
+            if (i == 0 || n0 + i < a.N) {
                 if constexpr (RHEAD) {
-                    cv = load_r<T, W, SCALAR>(c_p + int64_t(i) * a.H * a.r1_n);
-                    sv = load_r<T, W, SCALAR>(s_p + int64_t(i) * a.H * a.r2_n);
+                    cv = load_r<T, W, SCALAR>(c_p + int64_t(i) * a.r1_n);
+                    sv = load_r<T, W, SCALAR>(s_p + int64_t(i) * a.r2_n);
                 }
                 store_x<T, W, SCALAR>(xp[i], rotate_chunk<T, W, DIR>(xv[i], cv, sv));
             }

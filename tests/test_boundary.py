@@ -154,13 +154,15 @@ def test_plans_of_the_named_workloads(lib):
     # GQA fp16: 128-byte slices at offset 0 of 256-byte rows -> 16-byte accesses
     p = plan(lib, dtype=FP16, shape=(32, 2048, 16, 128), start=0, end=64, r_shape=(1, 2048, 1, 64))
     assert (p.path, p.vec_bytes, p.chunks_per_row, p.heads_per_thread, p.r_per_head) == (1, 16, 8, 4, 0)
-    assert p.tasks == 32 * 2048 * 4 * 8 and p.blocks == 152 * 8 and p.launches == 1
+    # 16-bit interleave: one block per 256 work items
+    assert p.tasks == 32 * 2048 * 4 * 8 and p.blocks == p.tasks // 256 and p.launches == 1
     # MLA-decode query bf16: one cos/sin row per token
     p = plan(lib, dtype=BF16, shape=(4096, 1, 128, 192), start=0, end=64, r_shape=(4096, 1, 1, 64))
     assert (p.path, p.vec_bytes, p.chunks_per_row, p.heads_per_thread) == (1, 16, 8, 4)
     # large fp32 with the slice at byte 136: 8-byte accesses hold whole pairs
     p = plan(lib, dtype=FP32, shape=(4, 8192, 32, 128), start=34, end=98, r_shape=(4, 8192, 1, 64))
     assert (p.path, p.vec_bytes, p.chunks_per_row, p.heads_per_thread) == (1, 8, 32, 2)
+    assert p.blocks == 152 * 8  # fp32: a resident grid that strides over the work
     # tiny fp32 and the small-model bf16 full-row slice
     p = plan(lib, dtype=FP32, shape=(1, 16, 2, 64), start=0, end=32, r_shape=(1, 16, 1, 32))
     assert (p.path, p.vec_bytes, p.heads_per_thread, p.blocks) == (1, 16, 1, 1)
