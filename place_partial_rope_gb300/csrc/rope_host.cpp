@@ -202,12 +202,13 @@ rope_status_t make_plan(int dir, int mode, int dtype, const Seg* seg, int nseg, 
     }
     P->r_head = R.rb[0][2] != 0 || R.rb[1][2] != 0;
     P->U = choose_heads_per_thread(N, heads_cap(half, e, P->vec, P->path));
-    // Grid: for 16-bit interleave rows a grid that covers the work once ran
-    // faster than a resident grid that strides over it (gqa 42.0 vs 44.7 us,
-    // 8- and 4-byte chunks 55-57 vs 61-62 us); fp32 rows and the half-split
-    // mode ran faster with the resident grid (fp32 8-byte chunks 103 vs
-    // 113 us, 16-byte chunks 87 vs 100 us).
-    P->full_grid = e == 2 && !half;
+    // Grid: for 16-bit interleave rows of one tensor a grid that covers the
+    // work once ran faster than a resident grid that strides over it (gqa
+    // 42.0 vs 44.7 us, 8- and 4-byte chunks 55-57 vs 61-62 us); fp32 rows,
+    // the half-split mode and the fused query + key call (22.5 vs 20.5 us)
+    // ran faster with the resident grid (fp32 8-byte chunks 103 vs 113 us,
+    // 16-byte chunks 87 vs 100 us).
+    P->full_grid = e == 2 && !half && nseg == 1;
     const int64_t H = (N + P->U - 1) / P->U;
     if (H * P->C > int64_t(kMaxPieceTasks))
         return fail(ROPE_ERR_INVALID, "N=%lld heads with a %lld-lane slice exceed the per-token work "
