@@ -66,6 +66,9 @@ def _open(path):
                                 ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64,
                                 ctypes.c_int64, ctypes.c_int64, ctypes.c_int64,
                                 i64p, i64p, i64p, i64p, ctypes.c_int64, ctypes.c_int64]
+    lib.oracle_rope_mixed.restype = ctypes.c_int
+    lib.oracle_rope_mixed.argtypes = [ctypes.c_int] * 5 + [ctypes.c_void_p] * 3 + \
+        [ctypes.c_int64] * 4 + [i64p] * 4 + [ctypes.c_int64] * 2
     for name in ("oracle_f32_to_bf16_n", "oracle_f32_to_f16_n",
                  "oracle_bf16_to_f32_n", "oracle_f16_to_f32_n"):
         fn = getattr(lib, name)
@@ -140,6 +143,50 @@ def fwd(x, r1, r2, dtype, start, end, formulation=GATHER_CHAIN, mode="interleave
 
 def bwd(g, r1, r2, dtype, start, end, formulation=GATHER_CHAIN, mode="interleave"):
     return rope(BWD, g, r1, r2, dtype, start, end, formulation, mode)
+
+
+def position_table(positions: np.ndarray, L: int, base: float, mode: str = "interleave"):
+    """cos/sin of every position, for the call that computes them in the
+    kernel: theta_k = p / base^(2k/L) for pair k in [0, L/2) ("ANE实战
+    RoPE位置编码在MIL中的纯ANE实现", sections 先搞懂RoPE and 第一步), computed in
+    float64 and rounded once to float32.  Pair k's value fills lanes 2k and
+    2k+1 (interleave) or k and k + L/2 (half).  Returns float32 arrays of
+    shape positions.shape + (1, L), i.e. (Bp, Sp, 1, L)."""
+    k = np.arange(L // 2, dtype=np.float64)
+    omega = np.power(float(base), -2.0 * k / L)
+    theta = positions.astype(np.float64)[..., None] * omega
+    c, s = np.cos(theta), np.sin(theta)
+    if mode == "half":
+        c, s = np.concatenate([c, c], axis=-1), np.concatenate([s, s], axis=-1)
+    else:
+        c, s = np.repeat(c, 2, axis=-1), np.repeat(s, 2, axis=-1)
+    c = np.ascontiguousarray(c.astype(np.float32)[..., None, :])
+    s = np.ascontiguousarray(s.astype(np.float32)[..., None, :])
+    return c, s
+
+
+def rope_pos(direction: int, x: np.ndarray, positions: np.ndarray, base: float, dtype: str,
+             start: int, end: int, mode: str = "interleave",
+             formulation: int = GATHER_CHAIN) -> np.ndarray:
+    """The operation with cos/sin computed from positions (one int32 per
+    (b, s), shape (Bp, Sp) broadcasting against (B, S)): the table of
+    position_table() -- float32 values, not rounded to x's type -- then the
+    same op chain as rope()."""
+    lib = _load()
+    code = DTYPE_CODES[dtype]
+    want = np.float32 if code == FP32 else np.uint16
+    if x.dtype != want or x.ndim != 4:
+        raise ValueError(f"oracle expects a 4-D {want} array for {dtype}")
+    c, s = position_table(np.asarray(positions), end - start, base, mode)
+    out = np.ascontiguousarray(x).copy()
+    B, S, N, D = out.shape
+    rc = lib.oracle_rope_mixed(direction, formulation, MODE_CODES[mode], code, FP32,
+                               out.ctypes.data, c.ctypes.data, s.ctypes.data, B, S, N, D,
+                               _i64x4(c.shape), _i64x4(_elem_strides(c)),
+                               _i64x4(s.shape), _i64x4(_elem_strides(s)), start, end)
+    if rc != 0:
+        raise ValueError("oracle rejected the arguments")
+    return out
 
 
 def rope_qk(direction: int, q: np.ndarray, k: np.ndarray, r1: np.ndarray, r2: np.ndarray,

@@ -293,11 +293,32 @@ static void row_pair_rotation(int dir, int mode, float* v, const float* c, const
  * rotation (1).  Returns 0, or -1 on arguments it does not accept (the
  * oracle checks only what it needs to stay in bounds).
  */
+int oracle_rope_mixed(int dir, int formulation, int mode, int dtype, int r_dtype, void* x,
+                      const void* r1, const void* r2, int64_t B, int64_t S, int64_t N, int64_t D,
+                      const int64_t* r1_shape, const int64_t* r1_stride,
+                      const int64_t* r2_shape, const int64_t* r2_stride,
+                      int64_t start, int64_t end);
+
 int oracle_rope(int dir, int formulation, int mode, int dtype, void* x, const void* r1,
                 const void* r2, int64_t B, int64_t S, int64_t N, int64_t D,
                 const int64_t* r1_shape, const int64_t* r1_stride,
                 const int64_t* r2_shape, const int64_t* r2_stride,
                 int64_t start, int64_t end)
+{
+    return oracle_rope_mixed(dir, formulation, mode, dtype, dtype, x, r1, r2, B, S, N, D,
+                             r1_shape, r1_stride, r2_shape, r2_stride, start, end);
+}
+
+/*
+ * oracle_rope_mixed: as oracle_rope, with cos/sin stored in their own type
+ * r_dtype (the in-kernel cos/sin of the positions call are fp32 values while
+ * x may be bf16 or fp16).
+ */
+int oracle_rope_mixed(int dir, int formulation, int mode, int dtype, int r_dtype, void* x,
+                      const void* r1, const void* r2, int64_t B, int64_t S, int64_t N, int64_t D,
+                      const int64_t* r1_shape, const int64_t* r1_stride,
+                      const int64_t* r2_shape, const int64_t* r2_stride,
+                      int64_t start, int64_t end)
 {
     const int64_t L = end - start;
     if (B < 0 || S < 0 || N < 0 || D < 0 || start < 0 || end > D || L < 0 || (L & 1))
@@ -333,8 +354,8 @@ int oracle_rope(int dir, int formulation, int mode, int dtype, void* x, const vo
                                    (r2_shape[2] == 1 ? 0 : n) * r2_stride[2];
                 for (int64_t j = 0; j < L; j++) {
                     v[j] = load_elem(x, row + j, dtype);
-                    c[j] = load_elem(r1, o1 + j * r1_stride[3], dtype);
-                    s[j] = load_elem(r2, o2 + j * r2_stride[3], dtype);
+                    c[j] = load_elem(r1, o1 + j * r1_stride[3], r_dtype);
+                    s[j] = load_elem(r2, o2 + j * r2_stride[3], r_dtype);
                 }
                 if (formulation == ORC_GATHER_CHAIN)
                     row_gather_chain(dir, mode, v, c, s, t1, t2, L);
