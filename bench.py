@@ -438,7 +438,36 @@ def breakdown(device, peak):
         del xd, gd, c, s
     out["mla_decode_qk"] = qk_breakdown(device, peak, flush)
     out["half_split"] = half_breakdown(device, peak, flush, l2)
+    out["positions"] = positions_breakdown(device, peak, flush, l2)
     torch.cuda.empty_cache()
+    return out
+
+
+def positions_breakdown(device, peak, flush, l2):
+    """cos/sin computed in the kernel from int32 positions (no table read)
+    on the three large shapes, forward, per launch.  The fraction is of the
+    bytes the positions call moves (the slice read + written, plus 4 bytes
+    per position)."""
+    from place_partial_rope_gb300 import binding
+    out = {}
+    for name in ("gqa", "mla_decode_q", "large_unaligned"):
+        w = synth.WORKLOADS[name]
+        x = synth.normal(w.shape, w.dtype, w.seed)
+        pos = np.ascontiguousarray(synth.positions(w)[..., 0], dtype=np.int32)
+        xd = synth.to_torch(x, w.dtype).to(device)
+        pd = torch.from_numpy(pos).to(device)
+        call = binding.PreparedPos("fwd", xd, pd, w.start, w.end)
+        for _ in range(3):
+            call()
+        nbytes = 2 * w.slice_elems() * synth.ELEM_BYTES[w.dtype] + pos.nbytes
+        t = time_launches(call, 30, flush)
+        e = {"cold_us": round(t * 1e6, 2), "cold_frac": round(nbytes / t / 1e9 / peak, 4)}
+        if nbytes > 1.5 * l2:
+            tb = time_back_to_back(call, 30)
+            e["steady_us"] = round(tb * 1e6, 2)
+            e["steady_frac"] = round(nbytes / tb / 1e9 / peak, 4)
+        out[name] = {"fwd": e}
+        del xd, pd
     return out
 
 

@@ -151,6 +151,47 @@ rope_status_t rope_partial_inplace_bwd_mode(void* grad, const void* r1, const vo
                                             rope_stream_t stream);
 
 /*
+ * rope_partial_inplace_fwd_pos / rope_partial_inplace_bwd_pos -- the same
+ * operations with cos and sin computed in the kernel from positions instead
+ * of read from r1 / r2.  The angle of pair k in [0, L/2) at position p is
+ * theta_k = p / base^(2k/L) (the RoPE definition and table recipe of
+ * "ANE实战 RoPE位置编码在MIL中的纯ANE实现", sections 先搞懂RoPE and 第一步,
+ * base 10000 there); both lanes of the pair use cos(theta_k) and
+ * sin(theta_k), i.e. the pair-duplicated table (interleave) or the
+ * half-duplicated one (half), without the table's bytes.
+ *
+ *   positions  device pointer to int32 positions, one per (batch, seq), of
+ *              shape pos_shape[0..1] (each 1 or B, S respectively) with
+ *              ELEMENT strides pos_stride[0..1]; read only.  Positions with
+ *              |p| < 2^24 are exact.
+ *   base       > 0 and finite (10000 in the usual recipe).
+ *   mode       ROPE_MODE_INTERLEAVE or ROPE_MODE_HALF.
+ *   other      as for rope_partial_inplace_fwd (x / grad, sizes, slice,
+ *              stream, asynchrony, the empty-call rule, status codes).
+ *
+ * Arithmetic: omega_k = base^(-2k/L) is computed on the host in double and
+ * passed as two fp32 parts; theta is formed and reduced by 2*pi in fp32
+ * arithmetic that keeps its error near 2^-22 (see the kernel), and sincosf
+ * gives cos and sin to within about 7e-7 of the exact values (for
+ * |p| < 2^24).  They stay in fp32 (they are not rounded to x's type); the
+ * rotation then rounds as above.  Results are therefore within that bound
+ * of the same operation with an fp32 table of correctly rounded cos/sin,
+ * not bit-identical to it.
+ */
+rope_status_t rope_partial_inplace_fwd_pos(void* x, const int32_t* positions, rope_dtype_t dtype,
+                                           int64_t B, int64_t S, int64_t N, int64_t D,
+                                           const int64_t pos_shape[2], const int64_t pos_stride[2],
+                                           double base, int64_t start, int64_t end,
+                                           rope_mode_t mode, rope_stream_t stream);
+
+rope_status_t rope_partial_inplace_bwd_pos(void* grad, const int32_t* positions,
+                                           rope_dtype_t dtype, int64_t B, int64_t S, int64_t N,
+                                           int64_t D, const int64_t pos_shape[2],
+                                           const int64_t pos_stride[2], double base,
+                                           int64_t start, int64_t end, rope_mode_t mode,
+                                           rope_stream_t stream);
+
+/*
  * rope_partial_inplace_fwd_qk / rope_partial_inplace_bwd_qk -- one launch
  * that rotates a query slice and a key slice with the same cos/sin rows: the
  * RoPE stage of MLA preprocessing, which applies the rotation to

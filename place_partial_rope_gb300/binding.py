@@ -78,6 +78,12 @@ def load_library() -> ctypes.CDLL:
     lib.rope_partial_plan_mode.restype = ctypes.c_int
     lib.rope_partial_plan_mode.argtypes = args + [ctypes.c_int, ctypes.c_int32,
                                                   ctypes.POINTER(RopePlan)]
+    pos_args = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int] + [ctypes.c_int64] * 4 + \
+        [i64p, i64p, ctypes.c_double, ctypes.c_int64, ctypes.c_int64, ctypes.c_int, ctypes.c_void_p]
+    for name in ("rope_partial_inplace_fwd_pos", "rope_partial_inplace_bwd_pos"):
+        fn = getattr(lib, name)
+        fn.restype = ctypes.c_int
+        fn.argtypes = pos_args
     qk = [ctypes.c_void_p] * 4 + [ctypes.c_int] + [ctypes.c_int64] * 10 + [i64p] * 4 + [ctypes.c_void_p]
     for name in ("rope_partial_inplace_fwd_qk", "rope_partial_inplace_bwd_qk"):
         fn = getattr(lib, name)
@@ -227,6 +233,59 @@ def rope_partial_inplace_bwd_qk(dq, dk, r1, r2, q_slice, k_slice, stream=None) -
     with torch.cuda.device(dq.device):
         st = lib.rope_partial_inplace_bwd_qk(*_qk_args(dq, dk, r1, r2, q_slice, k_slice, stream))
     _raise_for(lib, st)
+
+
+def _pos_args(x, positions, start, end, base, mode, stream):
+    if x.dim() != 4:
+        raise RopeError(ROPE_ERR_INVALID, f"x must be 4-D (B, S, N, D), got {x.dim()}-D")
+    if x.dtype not in DTYPE_CODE:
+        raise RopeError(ROPE_ERR_INVALID, f"unsupported dtype {x.dtype}")
+    if not x.is_contiguous() or not x.is_cuda:
+        raise RopeError(ROPE_ERR_INVALID, "x must be a contiguous CUDA tensor")
+    if positions.dim() != 2 or positions.dtype != torch.int32:
+        raise RopeError(ROPE_ERR_INVALID, "positions must be a 2-D int32 tensor (B|1, S|1)")
+    if not positions.is_cuda or positions.device != x.device:
+        raise RopeError(ROPE_ERR_INVALID, "positions must be on x's device")
+    p_shape = (ctypes.c_int64 * 2)(*positions.shape)
+    p_stride = (ctypes.c_int64 * 2)(*positions.stride())
+    return (x.data_ptr(), positions.data_ptr(), DTYPE_CODE[x.dtype], *x.shape, p_shape, p_stride,
+            float(base), int(start), int(end), _mode_code(mode), _stream_handle(stream, x.device))
+
+
+def rope_partial_inplace_fwd_pos(x, positions, start: int, end: int, base: float = 10000.0,
+                                 mode: str = "interleave", stream=None) -> None:
+    """Forward with cos/sin computed in the kernel from int32 positions of
+    shape (B|1, S|1): theta_k = p / base^(2k/L)."""
+    lib = load_library()
+    with torch.cuda.device(x.device):
+        st = lib.rope_partial_inplace_fwd_pos(*_pos_args(x, positions, start, end, base, mode, stream))
+    _raise_for(lib, st)
+
+
+def rope_partial_inplace_bwd_pos(grad, positions, start: int, end: int, base: float = 10000.0,
+                                 mode: str = "interleave", stream=None) -> None:
+    """Backward of rope_partial_inplace_fwd_pos, in place on the gradient."""
+    lib = load_library()
+    with torch.cuda.device(grad.device):
+        st = lib.rope_partial_inplace_bwd_pos(*_pos_args(grad, positions, start, end, base, mode,
+                                                          stream))
+    _raise_for(lib, st)
+
+
+class PreparedPos:
+    """rope_partial_inplace_{fwd,bwd}_pos with arguments marshalled once."""
+
+    def __init__(self, direction: str, x, positions, start, end, base=10000.0, mode="interleave",
+                 stream=None):
+        self._lib = load_library()
+        self._fn = getattr(self._lib, f"rope_partial_inplace_{direction}_pos")
+        self._keep = (x, positions)
+        self._args = _pos_args(x, positions, start, end, base, mode, stream)
+
+    def __call__(self) -> None:
+        st = self._fn(*self._args)
+        if st != ROPE_OK:
+            _raise_for(self._lib, st)
 
 
 class PreparedQK:

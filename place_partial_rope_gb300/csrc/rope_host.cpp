@@ -8,6 +8,7 @@
 // split of very large calls into launches whose flat work index fits 32 bits.
 // No CUDA call is made before the arguments have been validated, and none
 // at all for a rejected or empty call.
+#include <math.h>
 #include <stdarg.h>
 #include <stdint.h>
 #include <stdio.h>
@@ -288,12 +289,21 @@ int64_t r_extent(const Resolved& R, int r, const int64_t* shape) {
 }
 
 // Plan, size and launch every piece of a validated call.
+// The positions call's extra state: where the positions are and the
+// frequency table.
+struct PosCall {
+    const int32_t* pos;
+    int64_t pos_b, pos_s;  // element strides, 0 on broadcast dims
+    FreqTable freq;
+};
+
 rope_status_t launch_all(int dir, int mode, int dtype, const Seg* seg, int nseg, const void* r1,
                          const void* r2, const Resolved& R, int64_t B, int64_t S,
-                         rope_stream_t stream) {
+                         rope_stream_t stream, const PosCall* pc_pos = nullptr) {
     Plan P;
     rope_status_t st = make_plan(dir, mode, dtype, seg, nseg, r1, r2, R, &P);
     if (st != ROPE_OK) return st;
+    P.pos = pc_pos != nullptr;
 
     const char* err = nullptr;
     int sms = 0, bps = 0;
@@ -301,20 +311,28 @@ rope_status_t launch_all(int dir, int mode, int dtype, const Seg* seg, int nseg,
     if (kernel_blocks_per_sm(P, &bps, &err) != ROPE_OK) return fail(ROPE_ERR_CUDA, "%s", err);
     if (bps < 1) bps = 1;
 
-    const KernelArgs whole = base_args(P, seg, nseg, r1, r2, R);
+    KernelArgs whole = base_args(P, seg, nseg, r1, r2, R);
+    if (pc_pos) {
+        whole.pos = pc_pos->pos;
+        whole.pos_b = pc_pos->pos_b;
+        whole.pos_s = pc_pos->pos_s;
+        whole.pairs = static_cast<int32_t>(R.L / 2);
+    }
     const int64_t per_tok = int64_t(P.H) * P.C;
     return for_each_piece(B, S, per_tok, [&](const Piece& pc) -> rope_status_t {
         KernelArgs k = whole;
         const int64_t t0 = pc.b0 * S + pc.s0;
         k.x += t0 * whole.tok_bytes;
         if (k.x2) k.x2 += t0 * whole.tok_bytes2;
-        k.r1 += pc.b0 * whole.r1_b + pc.s0 * whole.r1_s;
-        k.r2 += pc.b0 * whole.r2_b + pc.s0 * whole.r2_s;
+        if (k.r1) k.r1 += pc.b0 * whole.r1_b + pc.s0 * whole.r1_s;
+        if (k.r2) k.r2 += pc.b0 * whole.r2_b + pc.s0 * whole.r2_s;
+        if (k.pos) k.pos += pc.b0 * whole.pos_b + pc.s0 * whole.pos_s;
         k.tasks = static_cast<uint32_t>(pc.count * per_tok);
         k.divS = FastDiv::make(static_cast<uint32_t>(pc.sp));
         const uint32_t blocks = static_cast<uint32_t>(grid_for(k.tasks, sms, bps, P.full_grid));
         const char* e2 = nullptr;
-        if (launch_piece(P, k, blocks, stream, &e2) != ROPE_OK) return fail(ROPE_ERR_CUDA, "%s", e2);
+        if (launch_piece(P, k, pc_pos ? &pc_pos->freq : nullptr, blocks, stream, &e2) != ROPE_OK)
+            return fail(ROPE_ERR_CUDA, "%s", e2);
         return ROPE_OK;
     });
 }
@@ -379,6 +397,54 @@ rope_status_t run_qk(int dir, void* q, void* k, const void* r1, const void* r2, 
     return launch_all(dir, kInterleave, dtype, seg, nseg, r1, r2, Rq.empty ? Rk : Rq, B, S, stream);
 }
 
+// The positions call: cos/sin of theta_k = p * base^(-2k/L) computed in
+// the kernel from one int32 position per (b, s).
+rope_status_t run_pos(int dir, void* x, const int32_t* positions, int dtype, int64_t B, int64_t S,
+                      int64_t N, int64_t D, const int64_t* pos_shape, const int64_t* pos_stride,
+                      double base, int64_t start, int64_t end, int mode, rope_stream_t stream) {
+    g_msg[0] = '\0';
+    if (mode != kInterleave && mode != kHalf)
+        return fail(ROPE_ERR_INVALID, "rotary mode %d is not interleave (1) or half (2)", mode);
+    if (!(base > 0.0) || !isfinite(base))
+        return fail(ROPE_ERR_INVALID, "base %g must be a finite number > 0", base);
+    // the x rules are those of the table call; a stand-in table of shape
+    // (1, 1, 1, L) lets check() apply them
+    const int64_t L = end - start;
+    const int64_t ones[4] = {1, 1, 1, L >= 0 ? L : 0};
+    const int64_t unit[4] = {0, 0, 0, 1};
+    Resolved R;
+    rope_status_t st = check(x, x, x, dtype, B, S, N, D, ones, unit, ones, unit, start, end, &R);
+    if (st != ROPE_OK || R.empty) return st;
+    if (!positions) return fail(ROPE_ERR_NULLPTR, "positions is null");
+    if (!pos_shape || !pos_stride) return fail(ROPE_ERR_NULLPTR, "pos_shape or pos_stride is null");
+    const int64_t xdim[2] = {B, S};
+    int64_t ps[2];
+    for (int k = 0; k < 2; ++k) {
+        if (!(pos_shape[k] == 1 || pos_shape[k] == xdim[k]))
+            return fail(ROPE_ERR_INVALID, "positions dim %d is %lld; it must be 1 or %lld", k,
+                        (long long)pos_shape[k], (long long)xdim[k]);
+        if (pos_shape[k] != 1 && pos_stride[k] < 0)
+            return fail(ROPE_ERR_INVALID, "positions stride %d is negative", k);
+        ps[k] = pos_shape[k] == 1 ? 0 : pos_stride[k];
+    }
+    if (reinterpret_cast<uintptr_t>(positions) % 4)
+        return fail(ROPE_ERR_INVALID, "positions must be 4-byte aligned int32");
+    if (L / 2 > kMaxPairs)
+        return fail(ROPE_ERR_INVALID, "slice length %lld exceeds %d", (long long)L, 2 * kMaxPairs);
+
+    PosCall pc{};
+    pc.pos = positions;
+    pc.pos_b = ps[0];
+    pc.pos_s = ps[1];
+    for (int64_t k = 0; k < L / 2; ++k) {
+        const double w = pow(base, -2.0 * double(k) / double(L));
+        pc.freq.hi[k] = static_cast<float>(w);
+        pc.freq.lo[k] = static_cast<float>(w - static_cast<double>(pc.freq.hi[k]));
+    }
+    const Seg seg{x, N, D, start};
+    return launch_all(dir, mode, dtype, &seg, 1, nullptr, nullptr, R, B, S, stream, &pc);
+}
+
 }  // namespace
 }  // namespace rope
 
@@ -422,6 +488,25 @@ rope_status_t rope_partial_inplace_bwd_mode(void* grad, const void* r1, const vo
                                             int64_t end, rope_mode_t mode, rope_stream_t stream) {
     return rope::run(rope::kBwd, grad, r1, r2, dtype, B, S, N, D, r1_shape, r1_stride, r2_shape,
                      r2_stride, start, end, stream, false, mode);
+}
+
+rope_status_t rope_partial_inplace_fwd_pos(void* x, const int32_t* positions, rope_dtype_t dtype,
+                                           int64_t B, int64_t S, int64_t N, int64_t D,
+                                           const int64_t pos_shape[2], const int64_t pos_stride[2],
+                                           double base, int64_t start, int64_t end,
+                                           rope_mode_t mode, rope_stream_t stream) {
+    return rope::run_pos(rope::kFwd, x, positions, dtype, B, S, N, D, pos_shape, pos_stride, base,
+                         start, end, mode, stream);
+}
+
+rope_status_t rope_partial_inplace_bwd_pos(void* grad, const int32_t* positions,
+                                           rope_dtype_t dtype, int64_t B, int64_t S, int64_t N,
+                                           int64_t D, const int64_t pos_shape[2],
+                                           const int64_t pos_stride[2], double base,
+                                           int64_t start, int64_t end, rope_mode_t mode,
+                                           rope_stream_t stream) {
+    return rope::run_pos(rope::kBwd, grad, positions, dtype, B, S, N, D, pos_shape, pos_stride,
+                         base, start, end, mode, stream);
 }
 
 rope_status_t rope_partial_inplace_fwd_qk(void* q, void* k, const void* r1, const void* r2,

@@ -11,6 +11,15 @@ namespace rope {
 constexpr int kThreads = 256;            // threads per block
 constexpr int kBlocksPerSmCap = 8;       // 2048 resident threads per SM / 256
 constexpr uint32_t kMaxPieceTasks = 1u << 31;  // flat work index of one launch
+constexpr int kMaxPairs = 512;           // L / 2 for the largest slice (D <= 1024)
+
+// Rotation frequencies of the positions call, omega_k = base^(-2k/L), each
+// as an fp32 pair hi + lo (hi = omega rounded to fp32, lo = the remainder
+// rounded to fp32), passed by value as the kernel's second parameter.
+struct FreqTable {
+    float hi[kMaxPairs];
+    float lo[kMaxPairs];
+};
 
 enum Direction : int { kFwd = 0, kBwd = 1 };
 enum Path : int { kNone = 0, kVector = 1, kScalarPair = 2 };
@@ -32,6 +41,9 @@ struct KernelArgs {
     int64_t tok_bytes2;        // token pitch of the second tensor
     int64_t row_bytes2;        // head pitch of the second tensor
     int64_t half_off;          // half-split mode: bytes from lane j to lane j + L/2
+    const int32_t* pos;        // positions call: position of the piece's first (b, s)
+    int64_t pos_b, pos_s;      // element strides of the positions (0: broadcast)
+    int32_t pairs;             // positions call: L / 2 entries of the FreqTable
     uint32_t tasks;            // work items of the piece: tokens * H * C
     int32_t N;                 // heads (first tensor's plus second tensor's)
     int32_t N1;                // heads of the first tensor
@@ -56,11 +68,13 @@ struct Plan {
     bool half;      // half-split mode (rope_partial_half_kernel)
     bool full_grid; // one block per 256 work items instead of a resident,
                     // grid-striding grid
+    bool pos;       // cos/sin computed from positions (rope_partial_pos_kernel)
 };
 
-// Launch one piece on `stream` with `blocks` blocks (defined in the .cu).
-rope_status_t launch_piece(const Plan& plan, const KernelArgs& args, uint32_t blocks,
-                           rope_stream_t stream, const char** err);
+// Launch one piece on `stream` with `blocks` blocks (defined in the .cu);
+// `freq` is the positions call's frequency table (nullptr otherwise).
+rope_status_t launch_piece(const Plan& plan, const KernelArgs& args, const FreqTable* freq,
+                           uint32_t blocks, rope_stream_t stream, const char** err);
 
 // A device address for the buffer [p, p + bytes) when the current device
 // can reach all of it (device, managed, page-locked host memory, or any host

@@ -473,15 +473,164 @@ __global__ void __launch_bounds__(kThreads) rope_partial_half_kernel(const Kerne
 }
 
 // ------------------------------------------------------------------------
+// cos/sin computed from positions (no table read)
+// ------------------------------------------------------------------------
+
+// 2*pi as three fp32 parts, each the fp32 rounding of what the parts before
+// it leave of 2*pi = 6.28318530717958647692528676655900576839... (remainder
+// after the three: 4.2e-23).  The first part's 24-bit significand makes
+// n * A exact inside an FMA for every |n| < 2^22.
+__device__ __forceinline__ float two_pi_a() { return __uint_as_float(0x40c90fdbu); }  //  6.2831855
+__device__ __forceinline__ float two_pi_b() { return __uint_as_float(0xb43bbd2eu); }  // -1.7484555e-07
+__device__ __forceinline__ float two_pi_c() { return __uint_as_float(0xa7f72cedu); }  // -6.8604980e-15
+__device__ __forceinline__ float inv_two_pi() { return __uint_as_float(0x3e22f983u); } //  0.15915494
+
+// cos and sin of theta = p * omega, omega = hi + lo.  theta is carried as
+// th + tl (th = p*hi rounded; tl = the exact residual of that product plus
+// p*lo), so it is accurate to about 2^-44 relative for |p| < 2^24 (p is
+// then exact in fp32).  Reduction by 2*pi follows Cody and Waite
+// ("Software Manual for the Elementary Functions", 1980) with the three-part
+// constant above: r = ((th - n*A) - n*B) - n*C + tl, where the first step is
+// exact (Sterbenz when |th| < 4, otherwise both terms are multiples of the
+// first part's ulp and the difference has at most 23 bits).  The other three
+// steps round once each, so |r - (theta - 2*pi*n)| <= 3 * 2^-23; sincosf adds
+// at most 2 ulp, and the cos/sin used are within about 7e-7 of the exact
+// values.
+__device__ __forceinline__ void angle_cos_sin(float p, float w_hi, float w_lo, float& c, float& s) {
+    const float th = __fmul_rn(p, w_hi);
+    const float tl = __fmaf_rn(p, w_lo, __fmaf_rn(p, w_hi, -th));
+    const float n = rintf(__fmul_rn(th, inv_two_pi()));
+    float r = __fmaf_rn(-n, two_pi_a(), th);
+    r = __fmaf_rn(-n, two_pi_b(), r);
+    r = __fmaf_rn(-n, two_pi_c(), r);
+    r = __fadd_rn(r, tl);
+    sincosf(r, &s, &c);
+}
+
+// Interleave mode: pair j of the chunk uses angle j.
+template <typename T, int W, int DIR>
+__device__ __forceinline__ Words<W> rotate_chunk_angles(const Words<W>& x, const float* cs,
+                                                        const float* sn) {
+    using P = Pack<T>;
+    constexpr int WPP = P::kWordsPerPair;
+    Words<W> y;
+#pragma unroll
+    for (int p = 0; p < W / WPP; ++p) {
+        float x0, x1, y0, y1;
+        P::get(&x.w[p * WPP], x0, x1);
+        rotate_pair<DIR>(x0, x1, cs[p], cs[p], sn[p], sn[p], y0, y1);
+        P::put(&y.w[p * WPP], y0, y1);
+    }
+    return y;
+}
+
+// Half-split mode: element k of chunk A and of chunk B use angle k.
+template <typename T, int W, bool SCALAR, int DIR>
+__device__ __forceinline__ void rotate_half_angles(const Words<W>& xa, const Words<W>& xb,
+                                                   const float* cs, const float* sn,
+                                                   Words<W>& ya, Words<W>& yb) {
+    if constexpr (SCALAR || sizeof(T) == 4) {
+#pragma unroll
+        for (int w = 0; w < W; ++w) {
+            float y0, y1;
+            rotate_pair<DIR>(Elem<T>::get(xa.w[w]), Elem<T>::get(xb.w[w]), cs[w], cs[w], sn[w],
+                             sn[w], y0, y1);
+            ya.w[w] = Elem<T>::put(y0);
+            yb.w[w] = Elem<T>::put(y1);
+        }
+    } else {
+        using P = Pack<T>;
+#pragma unroll
+        for (int w = 0; w < W; ++w) {
+            float a0, a1, b0, b1, ya0, ya1, yb0, yb1;
+            P::get(&xa.w[w], a0, a1);
+            P::get(&xb.w[w], b0, b1);
+            rotate_pair<DIR>(a0, b0, cs[2 * w], cs[2 * w], sn[2 * w], sn[2 * w], ya0, yb0);
+            rotate_pair<DIR>(a1, b1, cs[2 * w + 1], cs[2 * w + 1], sn[2 * w + 1], sn[2 * w + 1],
+                             ya1, yb1);
+            P::put(&ya.w[w], ya0, ya1);
+            P::put(&yb.w[w], yb0, yb1);
+        }
+    }
+}
+
+// The positions call: the task loop of rope_body with each chunk's cos/sin
+// computed once per thread (shared by its U heads) instead of loaded.
+template <typename T, int VEC, bool SCALAR, int U, int DIR, bool HALF>
+__global__ void __launch_bounds__(kThreads)
+rope_partial_pos_kernel(const KernelArgs a, const FreqTable f) {
+    __shared__ float w_hi[kMaxPairs];
+    __shared__ float w_lo[kMaxPairs];
+    for (int i = threadIdx.x; i < a.pairs; i += kThreads) {
+        w_hi[i] = f.hi[i];
+        w_lo[i] = f.lo[i];
+    }
+    __syncthreads();
+
+    constexpr int W = VEC >= 4 ? VEC / 4 : 1;
+    constexpr int E = VEC / int(sizeof(T)) > 0 ? VEC / int(sizeof(T)) : 1;  // elements per chunk
+    // angles per chunk: half-split one per element; interleave one per pair
+    constexpr int NA = HALF ? E : (E / 2 > 0 ? E / 2 : 1);
+    const uint64_t stride = uint64_t(gridDim.x) * kThreads;
+
+    for (uint64_t t = uint64_t(blockIdx.x) * kThreads + threadIdx.x; t < a.tasks; t += stride) {
+        uint32_t rest, c, tok, hg, b, s;
+        a.divC.divmod(uint32_t(t), rest, c);
+        a.divH.divmod(rest, tok, hg);
+        a.divS.divmod(tok, b, s);
+        const int n0 = int(hg) * U;
+        char* x0 = a.x + int64_t(tok) * a.tok_bytes + int64_t(n0) * a.row_bytes + int64_t(c) * VEC;
+
+        Words<W> xa[U], xb[U];
+#pragma unroll
+        for (int i = 0; i < U; ++i) {
+            if (i == 0 || n0 + i < a.N) {
+                if constexpr (HALF) {
+                    xa[i] = load_x_half<T, W, SCALAR>(x0 + i * a.row_bytes);
+                    xb[i] = load_x_half<T, W, SCALAR>(x0 + i * a.row_bytes + a.half_off);
+                } else {
+                    xa[i] = load_x<T, W, SCALAR>(x0 + i * a.row_bytes);
+                }
+            }
+        }
+
+        const float p = __int2float_rn(__ldg(a.pos + int64_t(b) * a.pos_b + int64_t(s) * a.pos_s));
+        const int k0 = int(c) * NA;
+        float cs[NA], sn[NA];
+#pragma unroll
+        for (int j = 0; j < NA; ++j) angle_cos_sin(p, w_hi[k0 + j], w_lo[k0 + j], cs[j], sn[j]);
+
+#pragma unroll
+        for (int i = 0; i < U; ++i) {
+            if (i == 0 || n0 + i < a.N) {
+                char* xp = x0 + i * a.row_bytes;
+                if constexpr (HALF) {
+                    Words<W> ya, yb;
+                    rotate_half_angles<T, W, SCALAR, DIR>(xa[i], xb[i], cs, sn, ya, yb);
+                    store_x_half<T, W, SCALAR>(xp, ya);
+                    store_x_half<T, W, SCALAR>(xp + a.half_off, yb);
+                } else {
+                    store_x<T, W, SCALAR>(xp, rotate_chunk_angles<T, W, DIR>(xa[i], cs, sn));
+                }
+            }
+        }
+    }
+}
+
+// ------------------------------------------------------------------------
 // kernel selection for one storage type (instantiated in one .cu per type)
 // ------------------------------------------------------------------------
 
-enum Kind { kSingle, kQK, kHalfSplit };
+enum Kind { kSingle, kQK, kHalfSplit, kPos, kPosHalf };
 
 template <typename T, int VEC, bool SCALAR, int U, Kind K>
 const void* pick_dir(const Plan& p) {
     const bool f = p.dir == kFwd;
-    if constexpr (K == kQK) {
+    if constexpr (K == kPos || K == kPosHalf) {
+        constexpr bool H = K == kPosHalf;
+        return f ? reinterpret_cast<const void*>(&rope_partial_pos_kernel<T, VEC, SCALAR, U, kFwd, H>)
+                 : reinterpret_cast<const void*>(&rope_partial_pos_kernel<T, VEC, SCALAR, U, kBwd, H>);
+    } else if constexpr (K == kQK) {
         return f ? reinterpret_cast<const void*>(&rope_partial_qk_kernel<T, VEC, SCALAR, U, kFwd>)
                  : reinterpret_cast<const void*>(&rope_partial_qk_kernel<T, VEC, SCALAR, U, kBwd>);
     } else if constexpr (K == kHalfSplit) {
@@ -528,23 +677,24 @@ const void* pick_interleave(const Plan& p) {
 }
 
 // Half-split mode: 16/8/4-byte chunks, or single 16-bit elements.
-template <typename T>
+template <typename T, Kind K>
 const void* pick_half(const Plan& p) {
     if (p.path == kScalarPair) {
-        if constexpr (sizeof(T) == 2) return pick_heads<T, 2, true, kHalfSplit>(p);
+        if constexpr (sizeof(T) == 2) return pick_heads<T, 2, true, K>(p);
         else return nullptr;  // an fp32 element is a 4-byte chunk
     }
     switch (p.vec) {
-        case 16: return pick_heads<T, 16, false, kHalfSplit>(p);
-        case 8: return pick_heads<T, 8, false, kHalfSplit>(p);
-        case 4: return pick_heads<T, 4, false, kHalfSplit>(p);
+        case 16: return pick_heads<T, 16, false, K>(p);
+        case 8: return pick_heads<T, 8, false, K>(p);
+        case 4: return pick_heads<T, 4, false, K>(p);
         default: return nullptr;
     }
 }
 
 template <typename T>
 const void* pick_kernel(const Plan& p) {
-    if (p.half) return pick_half<T>(p);
+    if (p.pos) return p.half ? pick_half<T, kPosHalf>(p) : pick_interleave<T, kPos>(p);
+    if (p.half) return pick_half<T, kHalfSplit>(p);
     if (p.two) return pick_interleave<T, kQK>(p);
     return pick_interleave<T, kSingle>(p);
 }

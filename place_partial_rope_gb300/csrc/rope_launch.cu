@@ -132,8 +132,8 @@ rope_status_t kernel_blocks_per_sm(const Plan& plan, int* blocks, const char** e
     return ROPE_OK;
 }
 
-rope_status_t launch_piece(const Plan& plan, const KernelArgs& args, uint32_t blocks,
-                           rope_stream_t stream, const char** err) {
+rope_status_t launch_piece(const Plan& plan, const KernelArgs& args, const FreqTable* freq,
+                           uint32_t blocks, rope_stream_t stream, const char** err) {
     const void* f = kernel_for(plan);
     if (!f) {
         *err = "internal error: no kernel instance for this plan";
@@ -141,7 +141,8 @@ rope_status_t launch_piece(const Plan& plan, const KernelArgs& args, uint32_t bl
     }
     if (blocks == 0) return ROPE_OK;
     KernelArgs a = args;
-    void* params[] = {&a};
+    // rope_partial_pos_kernel takes the frequency table as a second parameter
+    void* params[] = {&a, const_cast<FreqTable*>(freq)};
     const cudaError_t e = cudaLaunchKernel(f, dim3(blocks), dim3(kThreads), params, 0,
                                            reinterpret_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e, err);

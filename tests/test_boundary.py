@@ -64,6 +64,7 @@ def test_header_symbols_are_exported(lib):
                      "rope_partial_inplace_fwd_host", "rope_partial_inplace_bwd_host",
                      "rope_partial_inplace_fwd_qk", "rope_partial_inplace_bwd_qk",
                      "rope_partial_inplace_fwd_mode", "rope_partial_inplace_bwd_mode",
+                     "rope_partial_inplace_fwd_pos", "rope_partial_inplace_bwd_pos",
                      "rope_partial_plan_mode",
                      "rope_status_str", "rope_last_error_message", "rope_partial_plan"}
     for n in names:
@@ -312,3 +313,41 @@ def test_unknown_mode_rejected(lib, mode):
         st = fn(BASE, BASE + 2**30, BASE + 2**31, FP16, B, S, N, D, i64(*rs), i64(*contig(rs)),
                 i64(*rs), i64(*contig(rs)), 0, 8, mode, None)
         assert st == INVALID
+
+
+def pos_call(lib, fn="rope_partial_inplace_fwd_pos", x=BASE, pos=BASE + 2**30, dtype=FP16,
+             shape=(2, 4, 3, 16), p_shape=(2, 4), p_stride=(4, 1), base=10000.0, start=0, end=8,
+             mode=1):
+    B, S, N, D = shape
+    ps = (ctypes.c_int64 * 2)(*p_shape) if p_shape != "null" else None
+    pst = (ctypes.c_int64 * 2)(*p_stride)
+    return getattr(lib, fn)(x, pos, dtype, B, S, N, D, ps, pst, base, start, end, mode, None)
+
+
+@pytest.mark.parametrize("fn", ["rope_partial_inplace_fwd_pos", "rope_partial_inplace_bwd_pos"])
+@pytest.mark.parametrize("kwargs,status,needle", [
+    (dict(base=0.0), INVALID, "base"),
+    (dict(base=-2.0), INVALID, "base"),
+    (dict(base=float("nan")), INVALID, "base"),
+    (dict(base=float("inf")), INVALID, "base"),
+    (dict(mode=0), INVALID, "mode"),
+    (dict(pos=0), NULLPTR, "positions"),
+    (dict(p_shape="null"), NULLPTR, "pos_shape"),
+    (dict(p_shape=(3, 4)), INVALID, "positions dim 0"),
+    (dict(p_shape=(2, 2)), INVALID, "positions dim 1"),
+    (dict(p_stride=(-4, 1)), INVALID, "negative"),
+    (dict(pos=BASE + 2**30 + 2), INVALID, "aligned"),
+    (dict(x=0), NULLPTR, "x is null"),
+    (dict(start=1, end=8), INVALID, "even"),
+    (dict(shape=(2, 4, 3, 15)), INVALID, "even"),
+])
+def test_pos_rejected_calls(lib, fn, kwargs, status, needle):
+    st = pos_call(lib, fn, **kwargs)
+    assert st == status, (st, lib.rope_last_error_message())
+    assert needle in lib.rope_last_error_message().decode()
+
+
+def test_pos_empty_calls(lib):
+    assert pos_call(lib, start=4, end=4, x=0, pos=0, p_shape="null") == OK
+    assert pos_call(lib, shape=(0, 4, 3, 16), x=0, pos=0, p_shape=(1, 4)) == OK
+    assert pos_call(lib, p_shape=(1, 1), p_stride=(0, 0), start=4, end=4) == OK

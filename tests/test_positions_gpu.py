@@ -1,0 +1,117 @@
+"""GPU parity of the call that computes cos/sin from positions, against the
+oracle's fp64-derived fp32 table.
+
+The kernel's cos/sin are within about 7e-7 of the exact values (angle
+formed and reduced in fp32 with a three-part 2*pi, then sincosf), where the
+oracle uses the exact values rounded to fp32.  So the bar is a tolerance,
+derived from that bound: fp32 lanes within 1e-6 * (|x_m| + |x_n|) of the
+oracle plus 2 ulp for the final rounding; bf16 / fp16 lanes within one unit
+in the last place of the storage type.  Every byte outside the slice is
+bit-exact.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from gpu_util import DEV, to_dev
+from place_partial_rope_gb300 import binding, synth
+
+pytestmark = pytest.mark.gpu
+
+
+def split(a, mode):
+    if mode == "interleave":
+        return a[..., 0::2], a[..., 1::2]
+    h = a.shape[-1] // 2
+    return a[..., :h], a[..., h:]
+
+
+def ordered(bits16: np.ndarray) -> np.ndarray:
+    """16-bit float patterns -> integers in the order of their values."""
+    b = bits16.astype(np.int64)
+    return np.where(b & 0x8000, -(b & 0x7FFF), b)
+
+
+def assert_close(got, want, x, dtype, start, end, mode, what):
+    assert np.array_equal(got[..., :start].view(np.uint8), want[..., :start].view(np.uint8)), what
+    assert np.array_equal(got[..., end:].view(np.uint8), want[..., end:].view(np.uint8)), what
+    g, w = got[..., start:end], want[..., start:end]
+    if dtype == "fp32":
+        xs = x[..., start:end].astype(np.float64)
+        xm, xn = split(xs, mode)
+        mag = np.abs(xm) + np.abs(xn)
+        mag = np.concatenate([mag, mag], axis=-1) if mode == "half" else np.repeat(mag, 2, axis=-1)
+        tol = 1e-6 * mag + 2 * np.spacing(np.abs(w).astype(np.float32)).astype(np.float64)
+        err = np.abs(g.astype(np.float64) - w)
+        assert np.all(err <= tol), f"{what}: max err {err.max()}, worst ratio {(err / tol).max()}"
+    else:
+        d = np.abs(ordered(g) - ordered(w))
+        assert d.max() <= 1, f"{what}: {int((d > 1).sum())} lanes off by more than one ulp"
+        assert (d > 0).mean() < 0.02, f"{what}: {(d > 0).mean():.3%} of lanes differ"
+
+
+def run(direction, x, positions, dtype, start, end, mode, base=10000.0):
+    xd = to_dev(x, dtype)
+    pd = torch.from_numpy(np.ascontiguousarray(positions, dtype=np.int32)).to(DEV)
+    fn = binding.rope_partial_inplace_fwd_pos if direction == "fwd" else binding.rope_partial_inplace_bwd_pos
+    fn(xd, pd, start, end, base, mode)
+    torch.cuda.synchronize()
+    return synth.from_torch(xd)
+
+
+def check(direction, x, positions, dtype, start, end, mode, what, base=10000.0):
+    got = run(direction, x, positions, dtype, start, end, mode, base)
+    d = oracle.FWD if direction == "fwd" else oracle.BWD
+    want = oracle.rope_pos(d, x, positions, base, dtype, start, end, mode)
+    assert_close(got, want, oracle.widen(x, dtype), dtype, start, end, mode, what)
+
+
+@pytest.mark.parametrize("mode", ["interleave", "half"])
+@pytest.mark.parametrize("name", ["gqa", "mla_decode_q", "large_unaligned"])
+def test_named_shapes_with_positions(name, mode):
+    w = synth.WORKLOADS[name]
+    x = synth.normal(w.shape, w.dtype, w.seed)
+    pos = synth.positions(w)[..., 0].astype(np.int32)  # (Br, Sr) one position per (b, s)
+    for direction in w.directions:
+        inp = x if direction == "fwd" else synth.normal(w.shape, w.dtype, w.seed + 500)
+        check(direction, inp, pos, w.dtype, w.start, w.end, mode, f"{name} {mode} {direction}")
+
+
+SWEEP = [
+    ((2, 5, 3, 64), 0, 64, (2, 5)),
+    ((2, 5, 3, 64), 2, 58, (1, 5)),
+    ((2, 5, 3, 64), 3, 61, (2, 1)),        # odd start
+    ((3, 4, 7, 48), 1, 3, (1, 1)),         # one pair, one position for all
+    ((1, 7, 5, 1024), 0, 1024, (1, 7)),    # the largest slice: 512 angles
+    ((2, 3, 13, 24), 6, 22, (2, 3)),
+]
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "fp16", "fp32"])
+@pytest.mark.parametrize("mode", ["interleave", "half"])
+@pytest.mark.parametrize("k", range(len(SWEEP)))
+def test_positions_sweep(dtype, mode, k):
+    shape, st, en, pshape = SWEEP[k]
+    x = synth.normal(shape, dtype, 400 + k)
+    pos = np.random.default_rng(k).integers(0, 40000, size=pshape).astype(np.int32)
+    for direction in ("fwd", "bwd"):
+        check(direction, x, pos, dtype, st, en, mode, f"{shape} [{st},{en}) {direction}")
+
+
+@pytest.mark.parametrize("mode", ["interleave", "half"])
+def test_largest_exact_positions_and_other_bases(mode):
+    """Positions up to 2^24 - 1 (the largest exact in fp32), and bases other
+    than 10000."""
+    x = synth.normal((2, 6, 4, 64), "fp32", 7)
+    pos = np.array([[0, 1, 2**20, 2**23 + 3, 2**24 - 1, 12345],
+                    [-5, -2**22, 99, 7, 2**24 - 2, 500000]], np.int32)
+    for base in (10000.0, 500000.0, 2.0):
+        for direction in ("fwd", "bwd"):
+            check(direction, x, pos, "fp32", 0, 64, mode, f"base {base} {direction}", base)
+
+
+def test_position_zero_is_the_identity_on_the_gpu():
+    x = synth.normal((2, 3, 4, 32), "bf16", 3)
+    got = run("fwd", x, np.zeros((1, 1), np.int32), "bf16", 0, 32, "interleave")
+    assert np.array_equal(got, x)
