@@ -171,9 +171,9 @@ rope_status_t rope_partial_inplace_bwd_mode(void* grad, const void* r1, const vo
  *
  * Arithmetic: omega_k = base^(-2k/L) is computed on the host in double and
  * passed as two fp32 parts; theta is formed and reduced by 2*pi in fp32
- * arithmetic that keeps its error near 2^-22 (see the kernel), and sincosf
- * gives cos and sin to within about 7e-7 of the exact values (for
- * |p| < 2^24).  They stay in fp32 (they are not rounded to x's type); the
+ * arithmetic that keeps its error within 3 * 2^-23 (see the kernel), and the
+ * hardware sine/cosine on the reduced angle gives cos and sin to within
+ * 8e-7 of the exact values (for |p| < 2^24).  They stay in fp32 (they are not rounded to x's type); the
  * rotation then rounds as above.  Results are therefore within that bound
  * of the same operation with an fp32 table of correctly rounded cos/sin,
  * not bit-identical to it.
