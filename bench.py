@@ -605,7 +605,7 @@ def gpu_arm(args):
     ceiling = dense_rmw_ceiling(xd)
     out = {"metric": METRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": world,
            "steps": K, "warmup": args.warmup, "ms_per_step": round(1e3 * max_elapsed / K, 5),
-           "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "fp32",
+           "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": w.dtype,
            "data": "synthetic: seeded N(0,1) activations and gradients, base-10000 cos/sin table "
                    "at seeded per-batch position offsets",
            "config": workload_config(w, torch.cuda.get_device_properties(device).L2_cache_size),
@@ -739,7 +739,7 @@ def reference_arm(args):
     out = {"impl": "reference", "metric": METRIC, "value": round(base["value"], 4), "unit": "GB/s",
            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
            "ms_per_step": round(base["ms_per_step"], 3), "higher_is_better": True,
-           "scaling": "weak", "vs_baseline": None, "dtype": "fp32",
+           "scaling": "weak", "vs_baseline": None, "dtype": w.dtype,
            "data": "synthetic: seeded N(0,1) activations and gradients, base-10000 cos/sin table",
            "config": workload_config(w),
            "cpu_baseline": {k: base[k] for k in ("value", "unit", "cores", "kind", "sample")},

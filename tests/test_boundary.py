@@ -351,3 +351,21 @@ def test_pos_empty_calls(lib):
     assert pos_call(lib, start=4, end=4, x=0, pos=0, p_shape="null") == OK
     assert pos_call(lib, shape=(0, 4, 3, 16), x=0, pos=0, p_shape=(1, 4)) == OK
     assert pos_call(lib, p_shape=(1, 1), p_stride=(0, 0), start=4, end=4) == OK
+
+
+def test_cuda_failure_is_reported_not_raised(lib):
+    """A valid plan query with sm_count = 0 asks the current device.  Without
+    a usable GPU that query fails and comes back as ROPE_ERR_CUDA with a
+    message; with a GPU it succeeds.  Nothing is launched either way."""
+    import torch
+    B, S, N, D = 2, 4, 3, 16
+    rs = (1, S, 1, 8)
+    p = binding.RopePlan()
+    st = lib.rope_partial_plan(BASE, BASE + 2**30, BASE + 2**31, FP16, B, S, N, D, i64(*rs),
+                               i64(*contig(rs)), i64(*rs), i64(*contig(rs)), 0, 8, 0,
+                               ctypes.byref(p))
+    if torch.cuda.is_available():
+        assert st == OK and p.blocks > 0
+    else:
+        assert st == CUDA
+        assert lib.rope_last_error_message().decode() != ""
