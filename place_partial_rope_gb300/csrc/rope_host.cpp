@@ -161,7 +161,7 @@ struct Seg {
 };
 
 rope_status_t make_plan(int dir, int mode, int dtype, const Seg* seg, int nseg, const void* r1,
-                        const void* r2, const Resolved& R, Plan* P) {
+                        const void* r2, const Resolved& R, Plan* P, bool host = false) {
     const int e = R.e;
     const bool half = mode == kHalf;
     // interleave: an access holds whole pairs; half-split: an access holds
@@ -202,7 +202,10 @@ rope_status_t make_plan(int dir, int mode, int dtype, const Seg* seg, int nseg, 
         P->C = static_cast<int>(R.L / 2);
     }
     P->r_head = R.rb[0][2] != 0 || R.rb[1][2] != 0;
-    P->U = choose_heads_per_thread(N, heads_cap(half, e, P->vec, P->path));
+    // Host buffers (the *_host calls) are read across the host link, where
+    // one head per thread ran fastest: gqa 0.81 ms against 1.05 ms with 4;
+    // the large fp32 shape is link-bound at any value.
+    P->U = choose_heads_per_thread(N, host ? 1 : heads_cap(half, e, P->vec, P->path));
     // Grid: for 16-bit interleave rows of one tensor a grid that covers the
     // work once ran faster than a resident grid that strides over it (gqa
     // 42.0 vs 44.7 us, 8- and 4-byte chunks 55-57 vs 61-62 us); fp32 rows,
@@ -299,9 +302,10 @@ struct PosCall {
 
 rope_status_t launch_all(int dir, int mode, int dtype, const Seg* seg, int nseg, const void* r1,
                          const void* r2, const Resolved& R, int64_t B, int64_t S,
-                         rope_stream_t stream, const PosCall* pc_pos = nullptr) {
+                         rope_stream_t stream, const PosCall* pc_pos = nullptr,
+                         bool host = false) {
     Plan P;
-    rope_status_t st = make_plan(dir, mode, dtype, seg, nseg, r1, r2, R, &P);
+    rope_status_t st = make_plan(dir, mode, dtype, seg, nseg, r1, r2, R, &P, host);
     if (st != ROPE_OK) return st;
     P.pos = pc_pos != nullptr;
 
@@ -365,7 +369,7 @@ rope_status_t run(int dir, void* x, const void* r1, const void* r2, int dtype, i
         r2 = d2;
     }
     const Seg seg{x, N, D, start};
-    return launch_all(dir, mode, dtype, &seg, 1, r1, r2, R, B, S, stream);
+    return launch_all(dir, mode, dtype, &seg, 1, r1, r2, R, B, S, stream, nullptr, host_buffers);
 }
 
 // The fused query + key call: both tensors share B, S and each token's
