@@ -1,5 +1,9 @@
-// rope_kernels.cuh -- the sm_103a kernel of the in-place partial interleaved
-// rotary embedding, forward and backward, for bf16 / fp16 / fp32 storage.
+// rope_kernels.cuh -- the sm_103a kernels of the in-place partial rotary
+// embedding, forward and backward, for bf16 / fp16 / fp32 storage:
+//   rope_partial_kernel      one tensor, interleaved pairs (the page's mode)
+//   rope_partial_half_kernel one tensor, half-split pairs (i, i + L/2)
+//   rope_partial_qk_kernel   query and key in one launch, one cos/sin row
+//   rope_partial_pos_kernel  cos/sin computed from positions (no table)
 //
 // What it computes ("CANN ops-transformer inplace_partial_rotary_mul",
 // section 功能与计算公式, and its kernel op chain): for every row
@@ -14,11 +18,13 @@
 //
 // How (GB300): the op is a streaming read-modify-write of the slice bytes,
 // bound by HBM bandwidth, so there is no tensor-core work and no shared
-// memory.  One work item is (token, head group, chunk):
+// memory (except the positions kernel's 4 KB frequency table).  One work
+// item is (token, head group, chunk):
 //   * a chunk is one 16-, 8- or 4-byte access of x that holds whole pairs,
 //     so the pair swap happens inside a thread's registers (no shuffles);
 //     rows whose slice is not aligned for that fall back to a scalar path
-//     with one access per element ("scalar pair");
+//     with one access per element ("scalar pair"); in half-split mode a
+//     chunk of the slice's first half is paired with the chunk L/2 lanes on;
 //   * a thread keeps the chunk's cos/sin in registers and walks U
 //     consecutive heads of the same token (heads hg*U .. hg*U + U - 1),
 //     issuing all U loads of x before any arithmetic, so U accesses per
