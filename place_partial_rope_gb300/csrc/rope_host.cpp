@@ -587,6 +587,8 @@ rope_status_t rope_partial_plan_mode(const void* x, const void* r1, const void* 
     const Seg seg{const_cast<void*>(x), N, D, start};
     st = make_plan(kFwd, mode, dtype, &seg, 1, r1, r2, R, &P);
     if (st != ROPE_OK) return st;
+    if (!kernel_lookup(P))
+        return fail(ROPE_ERR_CUDA, "internal error: no kernel instance for this plan");
     int sms = sm_count, bps = kBlocksPerSmCap;
     if (sm_count <= 0) {
         const char* err = nullptr;

@@ -71,6 +71,10 @@ struct Plan {
     bool pos;       // cos/sin computed from positions (rope_partial_pos_kernel)
 };
 
+// The kernel instance a plan runs, or nullptr if none was compiled for it
+// (defined in the .cu; a table lookup, no CUDA call).
+const void* kernel_lookup(const Plan& plan);
+
 // Launch one piece on `stream` with `blocks` blocks (defined in the .cu);
 // `freq` is the positions call's frequency table (nullptr otherwise).
 rope_status_t launch_piece(const Plan& plan, const KernelArgs& args, const FreqTable* freq,

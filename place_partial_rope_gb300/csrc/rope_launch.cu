@@ -68,6 +68,8 @@ rope_status_t resolve_one(const void* p, const void** out, const char** err) {
 
 }  // namespace
 
+const void* kernel_lookup(const Plan& plan) { return kernel_for(plan); }
+
 rope_status_t device_address(const void* p, int64_t bytes, const void** out, const char** err) {
     const void* first = nullptr;
     const void* last = nullptr;

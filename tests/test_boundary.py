@@ -369,3 +369,30 @@ def test_cuda_failure_is_reported_not_raised(lib):
     else:
         assert st == CUDA
         assert lib.rope_last_error_message().decode() != ""
+
+
+@pytest.mark.parametrize("mode", [1, 2])
+@pytest.mark.parametrize("dtype", [BF16, FP16, FP32])
+def test_every_plan_has_a_kernel(lib, dtype, mode):
+    """Sweep slice offsets, lengths, head dims, head counts and pointer
+    alignments: every valid call's plan names a compiled kernel instance
+    (rope_partial_plan_mode reports a missing one as ROPE_ERR_CUDA)."""
+    e = 4 if dtype == FP32 else 2
+    count = 0
+    for D in (2, 6, 24, 64, 130, 1024):
+        for start in sorted({0, 1, 2, 3, 4, 8, D // 2 - (D // 2) % 2}):
+            for L in (2, 4, 6, 8, 16, 64, 1022):
+                end = start + L
+                if end > D:
+                    continue
+                for N in (1, 3, 8, 33):
+                    for xoff in (0, e, 4, 8):
+                        if xoff % e:
+                            continue
+                        st, p = plan_mode(lib, mode, x=BASE + xoff, dtype=dtype,
+                                          shape=(2, 3, N, D), start=start, end=end,
+                                          r_shape=(1, 3, 1, L))
+                        assert st == OK, (D, start, L, N, xoff, lib.rope_last_error_message())
+                        assert p.blocks > 0 and p.heads_per_thread in (1, 2, 4, 8)
+                        count += 1
+    assert count > 500
