@@ -292,7 +292,10 @@ def sample_bytes(w, tokens: int, r_rows: int) -> int:
     return len(w.directions) * (2 * tokens * N * w.L * e + 2 * r_rows * w.L * e)
 
 
-def time_oracle(w, x, r1, r2, g, steps: int, warmup: int, budget_s: float):
+def time_oracle(w, x, r1, r2, g, steps: int, warmup: int, budget_s: float, min_s: float = 0.0):
+    """Times the oracle over a sample of the workload: at least `steps`
+    steps, more (up to 1000) until about `min_s` seconds of wall time, and
+    the sample shrunk if `steps + warmup` of it would pass `budget_s`."""
     import oracle
     oracle.build()
     cores = host_cores()
@@ -308,10 +311,11 @@ def time_oracle(w, x, r1, r2, g, steps: int, warmup: int, budget_s: float):
         for _ in range(max(0, warmup - 1)):
             oracle_step(pool, cores, xs, c, s, gs, w)
         times = []
-        for _ in range(steps):
+        while len(times) < steps or (sum(times) < min_s and len(times) < 1000):
             t0 = time.perf_counter()
             oracle_step(pool, cores, xs, c, s, gs, w)
             times.append(time.perf_counter() - t0)
+        steps = len(times)
     per_step = sample_bytes(w, tokens, r_rows)
     total = sum(times)
     dirs = " + ".join({"fwd": "forward", "bwd": "backward"}[d] for d in w.directions)
@@ -619,7 +623,7 @@ def gpu_arm(args):
     if rank == 0:
         out["workloads"] = breakdown(device, peak)
     if rank == 0 and world == 1:
-        out["cpu_baseline"] = time_oracle(w, x, r1, r2, g, steps=20, warmup=1, budget_s=60.0)
+        out["cpu_baseline"] = time_oracle(w, x, r1, r2, g, steps=20, warmup=1, budget_s=60.0, min_s=10.0)
         out["cpu_baseline"].pop("ms_per_step", None)
     if rank == 0:
         print(json.dumps(out), flush=True)
