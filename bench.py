@@ -27,6 +27,7 @@ import ctypes
 import hashlib
 import json
 import os
+import platform
 import re
 import statistics
 import subprocess
@@ -326,6 +327,71 @@ def time_oracle(w, x, r1, r2, g, steps: int, warmup: int, budget_s: float, min_s
             "kind": "oracle", "sample": sample, "ms_per_step": 1e3 * total / steps}
 
 
+def cpu_model() -> str:
+    """The host CPU's model name (lscpu, else /proc/cpuinfo, else platform)."""
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.startswith("Model name:"):
+                return line.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    try:
+        for line in open("/proc/cpuinfo"):
+            if line.lower().startswith("model name"):
+                return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    return platform.processor() or platform.machine()
+
+
+def oracle_per_workload(names=("small_model", "gqa", "mla_decode_q", "large_unaligned"),
+                        sample_bytes_target: int = 16 * 2**20, reps: int = 5) -> dict:
+    """The oracle on each large workload and direction, on one thread and on
+    all host cores: the median of `reps` runs over a sample of the
+    workload's first tokens (about `sample_bytes_target` algorithmic bytes
+    per run).  A baseline only."""
+    import oracle
+    oracle.build()
+    cores = host_cores()
+    out = {}
+    with ThreadPoolExecutor(max_workers=cores) as pool:
+        for name in names:
+            w = synth.WORKLOADS[name]
+            x, r1, r2, g = synth.workload_inputs(w)
+            per_tok = 2 * w.shape[2] * w.L * synth.ELEM_BYTES[w.dtype]
+            tokens = int(min(w.tokens, max(1, sample_bytes_target // per_tok)))
+            xs, c, s, gs, r_rows = oracle_sample(w, x, r1, r2, g, tokens)
+            nbytes = sample_bytes(w, tokens, r_rows) // len(w.directions)
+            cuts = np.linspace(0, tokens, cores + 1).astype(int)
+            parts = [(a, b) for a, b in zip(cuts[:-1], cuts[1:]) if b > a]
+            entry = {"sample_tokens": tokens, "of_tokens": w.tokens}
+            for d in w.directions:
+                fn = oracle.fwd if d == "fwd" else oracle.bwd
+                arr = xs if d == "fwd" else gs
+
+                def one():
+                    fn(arr, c, s, w.dtype, w.start, w.end)
+
+                def many():
+                    list(pool.map(lambda ab: fn(arr[:, ab[0]:ab[1]], c[:, ab[0]:ab[1]],
+                                                s[:, ab[0]:ab[1]], w.dtype, w.start, w.end), parts))
+
+                res = {}
+                for label, f in (("1_thread", one), (f"{cores}_threads", many)):
+                    f()
+                    ts = []
+                    for _ in range(reps):
+                        t0 = time.perf_counter()
+                        f()
+                        ts.append(time.perf_counter() - t0)
+                    res[label + "_GB/s"] = round(nbytes / statistics.median(ts) / 1e9, 3)
+                entry[d] = res
+            out[name] = entry
+            del x, g
+    return out
+
+
 # --------------------------------------------------------------------------
 # the GPU arm
 # --------------------------------------------------------------------------
@@ -377,14 +443,19 @@ def time_launches(fn, n: int, flush=None):
     return statistics.median(a.elapsed_time(b) for a, b in evs) / 1e3
 
 
-def time_back_to_back(fn, n: int):
-    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    a.record()
-    for _ in range(n):
-        fn()
-    b.record()
-    torch.cuda.synchronize()
-    return a.elapsed_time(b) / 1e3 / n
+def time_back_to_back(fn, n: int, reps: int = 5):
+    """Per-launch device time (s) of n launches back to back between two
+    events; the median of `reps` repetitions."""
+    out = []
+    for _ in range(reps):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        for _ in range(n):
+            fn()
+        b.record()
+        torch.cuda.synchronize()
+        out.append(a.elapsed_time(b) / 1e3 / n)
+    return statistics.median(out)
 
 
 def time_graph(make_call, n: int, reps: int = 5):
@@ -428,12 +499,12 @@ def breakdown(device, peak):
             call = prep(buf, c, s, w.start, w.end)
             for _ in range(3):
                 call()
-            t = time_launches(call, 30, flush)
+            t = time_launches(call, 50, flush)
             gbs = w.algorithmic_bytes() / t / 1e9
             e = {"cold_us": round(t * 1e6, 2), "cold_GB/s": round(gbs, 1),
                  "cold_frac": round(gbs / peak, 4)}
             if w.algorithmic_bytes() > 1.5 * l2:
-                tb = time_back_to_back(call, 30)
+                tb = time_back_to_back(call, 50)
                 e["steady_us"] = round(tb * 1e6, 2)
                 e["steady_frac"] = round(w.algorithmic_bytes() / tb / 1e9 / peak, 4)
             e["graph_us"] = round(time_graph(lambda: prep(buf, c, s, w.start, w.end), 20) * 1e6, 2)
@@ -464,10 +535,10 @@ def positions_breakdown(device, peak, flush, l2):
         for _ in range(3):
             call()
         nbytes = 2 * w.slice_elems() * synth.ELEM_BYTES[w.dtype] + pos.nbytes
-        t = time_launches(call, 30, flush)
+        t = time_launches(call, 50, flush)
         e = {"cold_us": round(t * 1e6, 2), "cold_frac": round(nbytes / t / 1e9 / peak, 4)}
         if nbytes > 1.5 * l2:
-            tb = time_back_to_back(call, 30)
+            tb = time_back_to_back(call, 50)
             e["steady_us"] = round(tb * 1e6, 2)
             e["steady_frac"] = round(nbytes / tb / 1e9 / peak, 4)
         out[name] = {"fwd": e}
@@ -489,8 +560,8 @@ def half_breakdown(device, peak, flush, l2):
         call = binding.prepare_fwd(xd, c, s, w.start, w.end, mode="half")
         for _ in range(3):
             call()
-        t = time_launches(call, 30, flush)
-        tb = time_back_to_back(call, 30)
+        t = time_launches(call, 50, flush)
+        tb = time_back_to_back(call, 50)
         out[name] = {"fwd": {"cold_us": round(t * 1e6, 2),
                              "cold_frac": round(w.algorithmic_bytes() / t / 1e9 / peak, 4),
                              "steady_us": round(tb * 1e6, 2),
@@ -519,8 +590,8 @@ def qk_breakdown(device, peak, flush):
     for _ in range(3):
         fused()
         separate()
-    tf = time_launches(fused, 30, flush)
-    ts = time_launches(separate, 30, flush)
+    tf = time_launches(fused, 50, flush)
+    ts = time_launches(separate, 50, flush)
     nbytes = synth.qk_algorithmic_bytes()
     return {"fwd": {"fused_cold_us": round(tf * 1e6, 2), "separate_cold_us": round(ts * 1e6, 2),
                     "fused_GB/s": round(nbytes / tf / 1e9, 1),
@@ -625,6 +696,8 @@ def gpu_arm(args):
     if rank == 0 and world == 1:
         out["cpu_baseline"] = time_oracle(w, x, r1, r2, g, steps=20, warmup=1, budget_s=60.0, min_s=10.0)
         out["cpu_baseline"].pop("ms_per_step", None)
+        out["cpu_baseline"]["cpu_model"] = cpu_model()
+        out["cpu_baseline"]["workloads"] = oracle_per_workload()
     if rank == 0:
         print(json.dumps(out), flush=True)
     if world > 1:

@@ -272,6 +272,15 @@ def rope_partial_inplace_bwd_pos(grad, positions, start: int, end: int, base: fl
     _raise_for(lib, st)
 
 
+def _on_device(dev: int, fn, args) -> int:
+    """Call fn(*args) with `dev` as the current CUDA device (the device the
+    prepared tensors and stream belong to)."""
+    if torch.cuda.current_device() == dev:
+        return fn(*args)
+    with torch.cuda.device(dev):
+        return fn(*args)
+
+
 class PreparedPos:
     """rope_partial_inplace_{fwd,bwd}_pos with arguments marshalled once."""
 
@@ -281,9 +290,10 @@ class PreparedPos:
         self._fn = getattr(self._lib, f"rope_partial_inplace_{direction}_pos")
         self._keep = (x, positions)
         self._args = _pos_args(x, positions, start, end, base, mode, stream)
+        self._dev = x.device.index
 
     def __call__(self) -> None:
-        st = self._fn(*self._args)
+        st = _on_device(self._dev, self._fn, self._args)
         if st != ROPE_OK:
             _raise_for(self._lib, st)
 
@@ -296,9 +306,10 @@ class PreparedQK:
         self._fn = getattr(self._lib, f"rope_partial_inplace_{direction}_qk")
         self._keep = (q, k, r1, r2)
         self._args = _qk_args(q, k, r1, r2, q_slice, k_slice, stream)
+        self._dev = q.device.index
 
     def __call__(self) -> None:
-        st = self._fn(*self._args)
+        st = _on_device(self._dev, self._fn, self._args)
         if st != ROPE_OK:
             _raise_for(self._lib, st)
 
@@ -321,9 +332,10 @@ class PreparedCall:
         extra = () if mode is None else (_mode_code(mode),)
         self._args = (*_marshal(x, r1, r2, host=host), int(start), int(end), *extra,
                       _stream_handle(stream, dev))
+        self._dev = dev.index if dev.index is not None else torch.cuda.current_device()
 
     def __call__(self) -> None:
-        st = self._fn(*self._args)
+        st = _on_device(self._dev, self._fn, self._args)
         if st != ROPE_OK:
             _raise_for(self._lib, st)
 
