@@ -162,8 +162,11 @@ rope_status_t rope_partial_inplace_bwd_mode(void* grad, const void* r1, const vo
  *
  *   positions  device pointer to int32 positions, one per (batch, seq), of
  *              shape pos_shape[0..1] (each 1 or B, S respectively) with
- *              ELEMENT strides pos_stride[0..1]; read only.  Positions with
- *              |p| < 2^24 are exact.
+ *              ELEMENT strides pos_stride[0..1]; read only.  The error
+ *              bound below holds for |p| < 2^24, where p is exact in fp32;
+ *              a larger position is rounded to fp32 before use, and the
+ *              reduction by 2*pi then loses that bound (the call still
+ *              runs; nothing on the device checks the range).
  *   base       > 0 and finite (10000 in the usual recipe).
  *   mode       ROPE_MODE_INTERLEAVE or ROPE_MODE_HALF.
  *   other      as for rope_partial_inplace_fwd (x / grad, sizes, slice,
@@ -173,8 +176,8 @@ rope_status_t rope_partial_inplace_bwd_mode(void* grad, const void* r1, const vo
  * passed as two fp32 parts; theta is formed and reduced by 2*pi in fp32
  * arithmetic that keeps its error within 3 * 2^-23 (see the kernel), and the
  * hardware sine/cosine on the reduced angle gives cos and sin to within
- * 8e-7 of the exact values (for |p| < 2^24).  They stay in fp32 (they are not rounded to x's type); the
- * rotation then rounds as above.  Results are therefore within that bound
+ * 8e-7 of the exact values (for |p| < 2^24).  They stay in fp32 (they are
+ * not rounded to x's type); the rotation then rounds as above.  Results are therefore within that bound
  * of the same operation with an fp32 table of correctly rounded cos/sin,
  * not bit-identical to it.
  */
