@@ -818,7 +818,8 @@ def reference_arm(args):
            "ms_per_step": round(base["ms_per_step"], 3), "higher_is_better": True,
            "scaling": "weak", "vs_baseline": None, "dtype": w.dtype,
            "data": "synthetic: seeded N(0,1) activations and gradients, base-10000 cos/sin table",
-           "config": workload_config(w),
+           "config": workload_config(w, torch.cuda.get_device_properties(0).L2_cache_size
+                                     if torch.cuda.is_available() else 132 * 2**20),
            "cpu_baseline": {k: base[k] for k in ("value", "unit", "cores", "kind", "sample")},
            "e2e": {"value": round(base["value"], 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
                    "d2h_bytes_per_step": 0}}
