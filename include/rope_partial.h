@@ -280,7 +280,9 @@ const char* rope_last_error_message(void);
  * device.  No kernel is launched.
  */
 typedef struct {
-    int32_t path;             /* 0: no launch (empty), 1: vector kernel, 2: scalar-pair kernel */
+    int32_t path;             /* 0: no launch (empty), 1: vector kernel, 2: scalar-pair kernel, */
+                              /* 3: half-split vector kernel whose row of accesses fits one     */
+                              /* warp (the partner access comes from another lane)              */
     int32_t vec_bytes;        /* bytes per global access of x (16, 8 or 4; on the scalar path  */
                               /* a pair (interleave) or an element (half-split))                */
     int32_t heads_per_thread; /* heads one thread walks with its cos/sin kept in registers     */

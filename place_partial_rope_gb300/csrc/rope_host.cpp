@@ -130,10 +130,15 @@ rope_status_t check(const void* x, const void* r1, const void* r2, int dtype, in
 // The cap comes from back-to-back timings on GB300 of every access kind
 // (U = 1, 2, 4, 8 on the workloads' shapes).  fp32 rows want few heads per
 // thread: 16-byte chunks ran 87 us at U = 1 against 92 us at U = 4, and
-// 8-byte chunks 105 us at U = 2 against 115 us at U = 8 (half-split: U = 1,
-// 104 us against 112 us).  16-bit rows want 4: 16-byte chunks are flat from
-// U = 2 to 8 on 256-byte rows and best at 4 on 384-byte rows; 4-byte chunks
-// ran 62 us at U = 4 against 64 us at 8; the element path is best at 8.
+// 8-byte chunks 105 us at U = 2 against 115 us at U = 8 (half-split with
+// both halves in one thread: U = 1, 104 us against 112 us).  16-bit rows
+// want 4: 16-byte chunks are flat from U = 2 to 8 on 256-byte rows and best
+// at 4 on 384-byte rows; 4-byte chunks ran 62 us at U = 4 against 64 us at
+// 8; the element path is best at 8.  The half-split kernel whose partner
+// access comes from another lane moves the same accesses as interleave mode
+// and takes the interleave caps (`half` false): large fp32 shape 103 us at
+// U = 2 against 177 us at 1 and 110 us at 4; gqa 43 us at U = 4 against
+// 45 us at 2 and 51 us at 1.
 int heads_cap(bool half, int e, int vec, int path) {
     if (path == kScalarPair) return half ? 4 : 8;
     if (e == 4) {
@@ -161,7 +166,8 @@ struct Seg {
 };
 
 rope_status_t make_plan(int dir, int mode, int dtype, const Seg* seg, int nseg, const void* r1,
-                        const void* r2, const Resolved& R, Plan* P, bool host = false) {
+                        const void* r2, const Resolved& R, Plan* P, bool host = false,
+                        bool pos = false) {
     const int e = R.e;
     const bool half = mode == kHalf;
     // interleave: an access holds whole pairs; half-split: an access holds
@@ -201,18 +207,29 @@ rope_status_t make_plan(int dir, int mode, int dtype, const Seg* seg, int nseg, 
         P->vec = 2 * e;
         P->C = static_cast<int>(R.L / 2);
     }
+    P->pos = pos;
+    // Half-split rows of 2..32 accesses (a power of two) fit one warp: each
+    // thread then takes one access and its partner's comes by shuffle.  Back
+    // to back this ran the large fp32 shape in 102.9 us against 104.5-105.1
+    // us with both halves in one thread (the interleave kernel: 103.0 us),
+    // and gqa in 43.2 us against 44.6 us (interleave: 42.0 us); after an L2
+    // flush the two are level (gqa 40-41 us, large fp32 100-102 us).
+    const int64_t C_row = 2 * int64_t(P->C);
+    P->lanes = half && !pos && P->path == kVector && C_row <= 32 && (C_row & (C_row - 1)) == 0;
+    if (P->lanes) P->C = static_cast<int>(C_row);
     P->r_head = R.rb[0][2] != 0 || R.rb[1][2] != 0;
     // Host buffers (the *_host calls) are read across the host link, where
     // one head per thread ran fastest: gqa 0.81 ms against 1.05 ms with 4;
     // the large fp32 shape is link-bound at any value.
-    P->U = choose_heads_per_thread(N, host ? 1 : heads_cap(half, e, P->vec, P->path));
-    // Grid: for 16-bit interleave rows of one tensor a grid that covers the
-    // work once ran faster than a resident grid that strides over it (gqa
-    // 42.0 vs 44.7 us, 8- and 4-byte chunks 55-57 vs 61-62 us); fp32 rows,
-    // the half-split mode and the fused query + key call (22.5 vs 20.5 us)
-    // ran faster with the resident grid (fp32 8-byte chunks 103 vs 113 us,
-    // 16-byte chunks 87 vs 100 us).
-    P->full_grid = e == 2 && !half && nseg == 1;
+    P->U = choose_heads_per_thread(N, host ? 1 : heads_cap(half && !P->lanes, e, P->vec, P->path));
+    // Grid: for 16-bit rows of one tensor (interleave, or half-split with the
+    // partner in another lane) a grid that covers the work once ran faster
+    // than a resident grid that strides over it (gqa 42.0 vs 44.7 us, 8- and
+    // 4-byte chunks 55-57 vs 61-62 us; half-split gqa 43.4 vs 44.2 us); fp32
+    // rows, the half-split kernel that holds both halves and the fused
+    // query + key call (22.5 vs 20.5 us) ran faster with the resident grid
+    // (fp32 8-byte chunks 103 vs 113 us, 16-byte chunks 87 vs 100 us).
+    P->full_grid = e == 2 && (!half || P->lanes) && nseg == 1;
     const int64_t H = (N + P->U - 1) / P->U;
     if (H * P->C > int64_t(kMaxPieceTasks))
         return fail(ROPE_ERR_INVALID, "N=%lld heads with a %lld-lane slice exceed the per-token work "
@@ -305,9 +322,8 @@ rope_status_t launch_all(int dir, int mode, int dtype, const Seg* seg, int nseg,
                          rope_stream_t stream, const PosCall* pc_pos = nullptr,
                          bool host = false) {
     Plan P;
-    rope_status_t st = make_plan(dir, mode, dtype, seg, nseg, r1, r2, R, &P, host);
+    rope_status_t st = make_plan(dir, mode, dtype, seg, nseg, r1, r2, R, &P, host, pc_pos != nullptr);
     if (st != ROPE_OK) return st;
-    P.pos = pc_pos != nullptr;
 
     const char* err = nullptr;
     int sms = 0, bps = 0;
@@ -603,7 +619,7 @@ rope_status_t rope_partial_plan_mode(const void* x, const void* r1, const void* 
         ++launches;
         return ROPE_OK;
     });
-    plan->path = P.path;
+    plan->path = P.lanes ? 3 : P.path;
     plan->vec_bytes = P.vec;
     plan->heads_per_thread = P.U;
     plan->threads_per_block = kThreads;

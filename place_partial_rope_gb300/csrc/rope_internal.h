@@ -66,6 +66,9 @@ struct Plan {
     bool r_head;    // cos/sin differ between heads: reloaded per head
     bool two;       // fused query + key call (rope_partial_qk_kernel)
     bool half;      // half-split mode (rope_partial_half_kernel)
+    bool lanes;     // half-split with C accesses per row (a power of two in
+                    // [2, 32]), the partner access in lane ^ C/2
+                    // (rope_partial_half_lanes_kernel)
     bool full_grid; // one block per 256 work items instead of a resident,
                     // grid-striding grid
     bool pos;       // cos/sin computed from positions (rope_partial_pos_kernel)

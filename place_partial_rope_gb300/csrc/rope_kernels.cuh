@@ -2,6 +2,8 @@
 // embedding, forward and backward, for bf16 / fp16 / fp32 storage:
 //   rope_partial_kernel      one tensor, interleaved pairs (the page's mode)
 //   rope_partial_half_kernel one tensor, half-split pairs (i, i + L/2)
+//   rope_partial_half_lanes_kernel  the same when a row's accesses fit one
+//                            warp: the partner access comes by warp shuffle
 //   rope_partial_qk_kernel   query and key in one launch, one cos/sin row
 //   rope_partial_pos_kernel  cos/sin computed from positions (no table)
 //
@@ -479,6 +481,134 @@ __global__ void __launch_bounds__(kThreads) rope_partial_half_kernel(const Kerne
 }
 
 // ------------------------------------------------------------------------
+// half-split mode with the partner access in another lane
+// ------------------------------------------------------------------------
+// When a row's slice is C accesses long with C a power of two in [2, 32],
+// the work index puts the row's C accesses in C consecutive lanes of one
+// warp (C divides 32, so rows never straddle warps), and the access that
+// holds lane j + L/2 is the one C/2 lanes on.  Each thread then loads only
+// its own access of x, cos and sin, exactly as in interleave mode, and takes
+// the partner's x (and, in the backward, the partner's sin) with one warp
+// shuffle per 32-bit word.  Against pairing two accesses in one thread this
+// halves the registers per thread and lets 8 lanes cover a whole 128-byte
+// line of the slice.
+
+// One lane of a half-split pair, in the rounding order of rotate_pair.  For
+// the first-half lane j (own = x_j, other = x_{j+L/2}) and the second-half
+// lane j + L/2 (own = x_{j+L/2}, other = x_j), with c, s the own lane's
+// cos/sin and s_other the partner lane's sin:
+//   forward : first  own*c - other*s        second  own*c + other*s
+//   backward: first  own*c + other*s_other  second  own*c - other*s_other
+// Each is own*c + (±other)*s': the sign goes onto `other` before the
+// multiply (flipping sign bits is exact, fl(-a*b) = -fl(a*b), and a - b is
+// a + (-b) in IEEE arithmetic), so a lane costs what an interleaved pair
+// does: two products and one sum per element, plus one XOR per word.
+template <typename T, int W, int DIR>
+__device__ __forceinline__ Words<W> rotate_chunk_lanes(bool first, const Words<W>& x,
+                                                       const Words<W>& xo, const Words<W>& c,
+                                                       const Words<W>& s, const Words<W>& so) {
+    constexpr uint32_t kSign = sizeof(T) == 4 ? 0x80000000u : 0x80008000u;
+    const uint32_t neg = (DIR == kFwd) == first ? kSign : 0u;
+    const Words<W>& sx = DIR == kFwd ? s : so;
+    Words<W> y;
+    if constexpr (sizeof(T) == 4) {
+#pragma unroll
+        for (int w = 0; w < W; ++w)
+            y.w[w] = __float_as_uint(__fadd_rn(
+                __fmul_rn(__uint_as_float(x.w[w]), __uint_as_float(c.w[w])),
+                __fmul_rn(__uint_as_float(xo.w[w] ^ neg), __uint_as_float(sx.w[w]))));
+    } else {
+        // element k of a word pairs with element k of the partner's word
+        using P = Pack<T>;
+#pragma unroll
+        for (int w = 0; w < W; ++w) {
+            const uint32_t o = xo.w[w] ^ neg;
+            float x0, x1, o0, o1, c0, c1, s0, s1;
+            P::get(&x.w[w], x0, x1);
+            P::get(&o, o0, o1);
+            P::get(&c.w[w], c0, c1);
+            P::get(&sx.w[w], s0, s1);
+            P::put(&y.w[w], __fadd_rn(__fmul_rn(x0, c0), __fmul_rn(o0, s0)),
+                   __fadd_rn(__fmul_rn(x1, c1), __fmul_rn(o1, s1)));
+        }
+    }
+    return y;
+}
+
+template <int W>
+__device__ __forceinline__ Words<W> shfl_xor_words(uint32_t mask, const Words<W>& v, int lanes) {
+    Words<W> o;
+#pragma unroll
+    for (int w = 0; w < W; ++w) o.w[w] = __shfl_xor_sync(mask, v.w[w], lanes);
+    return o;
+}
+
+// One tensor, half-split mode, partner access in lane ^ C/2.
+template <typename T, int VEC, int U, int DIR, bool RHEAD>
+__global__ void __launch_bounds__(kThreads) rope_partial_half_lanes_kernel(const KernelArgs a) {
+    constexpr int W = VEC / 4;
+    constexpr int R = RHEAD ? U : 1;  // cos/sin accesses per thread
+    const uint32_t C = a.divC.d;      // accesses per row: a power of two in [2, 32]
+    const int other = int(C >> 1);    // lane distance to the partner access
+    const uint32_t lane = threadIdx.x & 31u;
+    const uint64_t stride = uint64_t(gridDim.x) * kThreads;
+
+    for (uint64_t t = uint64_t(blockIdx.x) * kThreads + threadIdx.x; t < a.tasks; t += stride) {
+        // the lanes of this warp still in the loop: items t - lane .. tasks - 1
+        // (tasks is a multiple of C, so a lane's partner is always among them)
+        const uint64_t left = a.tasks - (t - lane);
+        const uint32_t mask = left >= 32 ? 0xffffffffu : ((1u << uint32_t(left)) - 1u);
+        uint32_t rest, c, tok, hg, b, s;
+        a.divC.divmod(uint32_t(t), rest, c);
+        a.divH.divmod(rest, tok, hg);
+        a.divS.divmod(tok, b, s);
+        const bool first = c < C / 2;
+        const int n0 = int(hg) * U;
+        const int64_t c_off = int64_t(c) * VEC;
+        char* x0 = a.x + int64_t(tok) * a.tok_bytes + int64_t(n0) * a.row_bytes + c_off;
+        const char* c_p = a.r1 + int64_t(b) * a.r1_b + int64_t(s) * a.r1_s + c_off;
+        const char* s_p = a.r2 + int64_t(b) * a.r2_b + int64_t(s) * a.r2_s + c_off;
+        if constexpr (RHEAD) {
+            c_p += int64_t(n0) * a.r1_n;
+            s_p += int64_t(n0) * a.r2_n;
+        }
+
+        // loads (heads past N read nothing and hold zeros)
+        Words<W> xv[U];
+#pragma unroll
+        for (int i = 0; i < U; ++i) {
+            if (i == 0 || n0 + i < a.N) xv[i] = load_x<T, W, false>(x0 + i * a.row_bytes);
+            else xv[i] = Words<W>{};
+        }
+        Words<W> cv[R], sv[R];
+#pragma unroll
+        for (int j = 0; j < R; ++j) {
+            if (j == 0 || n0 + j < a.N) {
+                cv[j] = load_r<T, W, false>(c_p + int64_t(j) * a.r1_n);
+                sv[j] = load_r<T, W, false>(s_p + int64_t(j) * a.r2_n);
+            } else {
+                cv[j] = Words<W>{};
+                sv[j] = Words<W>{};
+            }
+        }
+        // the partner's values: every lane of `mask` shuffles, outside any
+        // per-lane condition
+        Words<W> so[R];
+#pragma unroll
+        for (int j = 0; j < R; ++j) so[j] = DIR == kBwd ? shfl_xor_words<W>(mask, sv[j], other) : sv[j];
+#pragma unroll
+        for (int i = 0; i < U; ++i) {
+            const Words<W> xo = shfl_xor_words<W>(mask, xv[i], other);
+            if (i == 0 || n0 + i < a.N) {
+                const int j = RHEAD ? i : 0;
+                store_x<T, W, false>(x0 + i * a.row_bytes,
+                                     rotate_chunk_lanes<T, W, DIR>(first, xv[i], xo, cv[j], sv[j], so[j]));
+            }
+        }
+    }
+}
+
+// ------------------------------------------------------------------------
 // cos/sin computed from positions (no table read)
 // ------------------------------------------------------------------------
 
@@ -629,7 +759,7 @@ rope_partial_pos_kernel(const KernelArgs a, const FreqTable f) {
 // kernel selection for one storage type (instantiated in one .cu per type)
 // ------------------------------------------------------------------------
 
-enum Kind { kSingle, kQK, kHalfSplit, kPos, kPosHalf };
+enum Kind { kSingle, kQK, kHalfSplit, kHalfLanes, kPos, kPosHalf };
 
 template <typename T, int VEC, bool SCALAR, int U, Kind K>
 const void* pick_dir(const Plan& p) {
@@ -641,6 +771,12 @@ const void* pick_dir(const Plan& p) {
     } else if constexpr (K == kQK) {
         return f ? reinterpret_cast<const void*>(&rope_partial_qk_kernel<T, VEC, SCALAR, U, kFwd>)
                  : reinterpret_cast<const void*>(&rope_partial_qk_kernel<T, VEC, SCALAR, U, kBwd>);
+    } else if constexpr (K == kHalfLanes) {
+        if (f)
+            return p.r_head ? reinterpret_cast<const void*>(&rope_partial_half_lanes_kernel<T, VEC, U, kFwd, true>)
+                            : reinterpret_cast<const void*>(&rope_partial_half_lanes_kernel<T, VEC, U, kFwd, false>);
+        return p.r_head ? reinterpret_cast<const void*>(&rope_partial_half_lanes_kernel<T, VEC, U, kBwd, true>)
+                        : reinterpret_cast<const void*>(&rope_partial_half_lanes_kernel<T, VEC, U, kBwd, false>);
     } else if constexpr (K == kHalfSplit) {
         if (f)
             return p.r_head ? reinterpret_cast<const void*>(&rope_partial_half_kernel<T, VEC, SCALAR, U, kFwd, true>)
@@ -684,6 +820,18 @@ const void* pick_interleave(const Plan& p) {
     }
 }
 
+// Half-split mode with the partner access in another lane: 16/8/4-byte
+// accesses.
+template <typename T>
+const void* pick_half_lanes(const Plan& p) {
+    switch (p.vec) {
+        case 16: return pick_heads<T, 16, false, kHalfLanes>(p);
+        case 8: return pick_heads<T, 8, false, kHalfLanes>(p);
+        case 4: return pick_heads<T, 4, false, kHalfLanes>(p);
+        default: return nullptr;
+    }
+}
+
 // Half-split mode: 16/8/4-byte chunks, or single 16-bit elements.
 template <typename T, Kind K>
 const void* pick_half(const Plan& p) {
@@ -702,7 +850,7 @@ const void* pick_half(const Plan& p) {
 template <typename T>
 const void* pick_kernel(const Plan& p) {
     if (p.pos) return p.half ? pick_half<T, kPosHalf>(p) : pick_interleave<T, kPos>(p);
-    if (p.half) return pick_half<T, kHalfSplit>(p);
+    if (p.half) return p.lanes ? pick_half_lanes<T>(p) : pick_half<T, kHalfSplit>(p);
     if (p.two) return pick_interleave<T, kQK>(p);
     return pick_interleave<T, kSingle>(p);
 }

@@ -284,23 +284,37 @@ def plan_mode(lib, mode, x=BASE, r1=BASE + 2**30, r2=BASE + 2**31, dtype=FP16, s
 
 
 def test_half_split_plans(lib):
-    HALF = 2
-    # gqa-like fp16: each half of the 64-lane slice is 64 bytes -> 16-byte chunks
+    HALF, LANES = 2, 3
+    # gqa-like fp16: the 64-lane slice is 8 accesses of 16 bytes, one warp's
+    # worth, so the partner access (4 lanes on) comes by shuffle; 4 heads per
+    # thread and one block per 256 items, as in interleave mode
     st, p = plan_mode(lib, HALF, shape=(32, 2048, 16, 128), start=0, end=64, r_shape=(1, 2048, 1, 64))
-    assert st == OK and (p.path, p.vec_bytes, p.chunks_per_row, p.heads_per_thread) == (1, 16, 4, 4)
-    # fp32 slice at byte 136: each half 128 bytes, chunks of 8 bytes (one pair of lanes per half)
+    assert st == OK and (p.path, p.vec_bytes, p.chunks_per_row, p.heads_per_thread) == (LANES, 16, 8, 4)
+    assert p.blocks == p.tasks // 256
+    # fp32 slice at byte 136: 8-byte accesses (each half is 128 bytes), 32 per row
     st, p = plan_mode(lib, HALF, dtype=FP32, shape=(4, 8192, 32, 128), start=34, end=98,
                       r_shape=(4, 8192, 1, 64))
-    assert st == OK and (p.path, p.vec_bytes, p.chunks_per_row) == (1, 8, 16)
-    # fp16 odd start: single elements
+    assert st == OK and (p.path, p.vec_bytes, p.chunks_per_row, p.heads_per_thread) == (LANES, 8, 32, 2)
+    assert p.blocks == 152 * 8   # fp32 rows: the resident grid
+    # fp16 odd start: single elements, both halves in one thread
     st, p = plan_mode(lib, HALF, start=1, end=9)
     assert st == OK and (p.path, p.vec_bytes, p.chunks_per_row) == (2, 2, 4)
-    # fp32 odd start: a 4-byte chunk is one element
+    # fp32 odd start: a 4-byte access is one element; 8 per row
     st, p = plan_mode(lib, HALF, dtype=FP32, start=1, end=9)
-    assert st == OK and (p.path, p.vec_bytes, p.chunks_per_row) == (1, 4, 4)
-    # half of L = 2 lanes of fp16 is 4 bytes
+    assert st == OK and (p.path, p.vec_bytes, p.chunks_per_row) == (LANES, 4, 8)
+    # half of L = 2 lanes of fp16 is 4 bytes: 2 accesses per row
     st, p = plan_mode(lib, HALF, start=0, end=4)
-    assert st == OK and (p.path, p.vec_bytes, p.chunks_per_row) == (1, 4, 1)
+    assert st == OK and (p.path, p.vec_bytes, p.chunks_per_row) == (LANES, 4, 2)
+    # 6 accesses per row (not a power of two): both halves in one thread
+    st, p = plan_mode(lib, HALF, shape=(2, 4, 3, 64), start=0, end=48)
+    assert st == OK and (p.path, p.vec_bytes, p.chunks_per_row) == (1, 16, 3)
+    # 128 accesses per row (more than a warp): both halves in one thread,
+    # 64 accesses of the first half
+    st, p = plan_mode(lib, HALF, dtype=FP32, shape=(2, 4, 3, 512), start=0, end=512)
+    assert st == OK and (p.path, p.vec_bytes, p.chunks_per_row) == (1, 16, 64)
+    # 32 accesses per row: the largest that fits one warp
+    st, p = plan_mode(lib, HALF, dtype=FP32, shape=(2, 4, 3, 128), start=0, end=128)
+    assert st == OK and (p.path, p.vec_bytes, p.chunks_per_row) == (LANES, 16, 32)
 
 
 @pytest.mark.parametrize("mode", [0, 3, -1])

@@ -1,5 +1,8 @@
 """GPU parity of the half-split rotary mode (pairs (i, i + L/2)) against the
-CPU oracle, bit for bit, including every byte outside the slice."""
+CPU oracle, bit for bit, including every byte outside the slice.  The sweep
+covers both half-split kernels: rows of 2..32 accesses (a power of two),
+where the partner access comes from another lane, and the rest, where one
+thread holds both halves."""
 import numpy as np
 import pytest
 import torch
@@ -36,6 +39,14 @@ SWEEP = [
     ((2, 3, 13, 24), 6, 22, "1SND"),       # ragged heads
     ((4, 9, 1, 10), 0, 10, "BS1D"),        # N = 1, 5-lane halves
     ((3, 1, 128, 192), 0, 64, "B11D"),     # MLA-like rows
+    # rows of 2..32 accesses (a power of two): the partner access comes from
+    # another lane of the warp
+    ((2, 5, 6, 64), 0, 64, "BSND"),        # cos/sin per head, idle head slots
+    ((3, 7, 5, 128), 0, 128, "1S1D"),      # fp32: 32 accesses per row
+    ((1, 3, 3, 8), 0, 8, "BS1D"),          # 2 accesses per row
+    ((1, 1, 3, 64), 0, 64, "BS1D"),        # 16 work items: a partial warp
+    ((1, 3, 5, 32), 0, 32, "B1ND"),        # partial warps, cos/sin per head
+    ((2, 3, 4, 40), 4, 36, "BS1D"),        # 16-bit: 8-byte accesses
 ]
 
 
