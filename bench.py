@@ -520,28 +520,31 @@ def breakdown(device, peak):
 
 def positions_breakdown(device, peak, flush, l2):
     """cos/sin computed in the kernel from int32 positions (no table read)
-    on the three large shapes, forward, per launch.  The fraction is of the
-    bytes the positions call moves (the slice read + written, plus 4 bytes
-    per position)."""
+    on the three large shapes, forward, per launch (interleave mode; the
+    gqa and large fp32 shapes also in half-split mode).  The fraction is of
+    the bytes the positions call moves (the slice read + written, plus 4
+    bytes per position)."""
     from place_partial_rope_gb300 import binding
     out = {}
-    for name in ("gqa", "mla_decode_q", "large_unaligned"):
+    for name, modes in (("gqa", ("interleave", "half")), ("mla_decode_q", ("interleave",)),
+                        ("large_unaligned", ("interleave", "half"))):
         w = synth.WORKLOADS[name]
         x = synth.normal(w.shape, w.dtype, w.seed)
         pos = np.ascontiguousarray(synth.positions(w)[..., 0], dtype=np.int32)
         xd = synth.to_torch(x, w.dtype).to(device)
         pd = torch.from_numpy(pos).to(device)
-        call = binding.PreparedPos("fwd", xd, pd, w.start, w.end)
-        for _ in range(3):
-            call()
         nbytes = 2 * w.slice_elems() * synth.ELEM_BYTES[w.dtype] + pos.nbytes
-        t = time_launches(call, 50, flush)
-        e = {"cold_us": round(t * 1e6, 2), "cold_frac": round(nbytes / t / 1e9 / peak, 4)}
-        if nbytes > 1.5 * l2:
-            tb = time_back_to_back(call, 50)
-            e["steady_us"] = round(tb * 1e6, 2)
-            e["steady_frac"] = round(nbytes / tb / 1e9 / peak, 4)
-        out[name] = {"fwd": e}
+        for mode in modes:
+            call = binding.PreparedPos("fwd", xd, pd, w.start, w.end, mode=mode)
+            for _ in range(3):
+                call()
+            t = time_launches(call, 50, flush)
+            e = {"cold_us": round(t * 1e6, 2), "cold_frac": round(nbytes / t / 1e9 / peak, 4)}
+            if nbytes > 1.5 * l2:
+                tb = time_back_to_back(call, 50)
+                e["steady_us"] = round(tb * 1e6, 2)
+                e["steady_frac"] = round(nbytes / tb / 1e9 / peak, 4)
+            out[name if mode == "interleave" else f"{name}/half"] = {"fwd": e}
         del xd, pd
     return out
 
