@@ -213,7 +213,10 @@ rope_status_t make_plan(int dir, int mode, int dtype, const Seg* seg, int nseg, 
     // to back this ran the large fp32 shape in 102.9 us against 104.5-105.1
     // us with both halves in one thread (the interleave kernel: 103.0 us),
     // and gqa in 43.2 us against 44.6 us (interleave: 42.0 us); after an L2
-    // flush the two are level (gqa 40-41 us, large fp32 100-102 us).
+    // flush the two are level (gqa 40-41 us, large fp32 100-102 us).  The
+    // positions call keeps both halves in one thread: there each lane would
+    // compute its partner's angles again, and the large fp32 shape ran 105.0
+    // us that way against 103.9 us (gqa level at 47.3 against 47.8 us).
     const int64_t C_row = 2 * int64_t(P->C);
     P->lanes = half && !pos && P->path == kVector && C_row <= 32 && (C_row & (C_row - 1)) == 0;
     if (P->lanes) P->C = static_cast<int>(C_row);
