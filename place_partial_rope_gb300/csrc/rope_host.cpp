@@ -128,24 +128,32 @@ rope_status_t check(const void* x, const void* r1, const void* r2, int dtype, in
 // flight, cos/sin reused more) wins over a perfect fit.
 //
 // The cap comes from back-to-back timings on GB300 of every access kind
-// (U = 1, 2, 4, 8 on the workloads' shapes).  fp32 rows want few heads per
-// thread: 16-byte chunks ran 87 us at U = 1 against 92 us at U = 4, and
-// 8-byte chunks 105 us at U = 2 against 115 us at U = 8 (half-split with
-// both halves in one thread: U = 1, 104 us against 112 us).  16-bit rows
-// want 4: 16-byte chunks are flat from U = 2 to 8 on 256-byte rows and best
-// at 4 on 384-byte rows; 4-byte chunks ran 62 us at U = 4 against 64 us at
-// 8; the element path is best at 8.  The half-split kernel whose partner
-// access comes from another lane moves the same accesses as interleave mode
-// and takes the interleave caps (`half` false): large fp32 shape 103 us at
-// U = 2 against 177 us at 1 and 110 us at 4; gqa 43 us at U = 4 against
-// 45 us at 2 and 51 us at 1.
-int heads_cap(bool half, int e, int vec, int path) {
-    if (path == kScalarPair) return half ? 4 : 8;
+// (U = 1, 2, 4, 8, and both grids, on the workloads' shapes and on other
+// slices of them).  fp32 rows want about 32 bytes of x per thread: 8-byte
+// accesses of the large shape's slice at byte 136 ran 99.5 us at U = 4
+// against 110.8 us at 2 and 100.4 us at 8 (the positions call: 97.1 us);
+// 16-byte accesses ran 82.7 us at U = 2 against 83.2 us at 4 ([32, 96))
+// and 159.7 against 160.0 us (the whole 512-byte row).  A thread that holds
+// both halves of a half-split pair moves two accesses per head, so it takes
+// half of that ([2, 98), 8-byte accesses: 135 us at U = 2 against 203 us at
+// 1; [1, 97), 4-byte: 156 us at U = 4 against 257 us at 1).  16-bit rows:
+// 16-byte accesses want 4 (gqa 42.0 us; flat from 2 to 8 on 256-byte rows,
+// best at 4 on 384-byte rows), 8-byte ones 2 (55.5 us against 57.7 at 4)
+// and 4-byte ones 4 (57.5 us against 71.9 at 2).  The half-split kernel that
+// takes its partner from another lane wants more in flight (8-byte accesses
+// 56.5 us at U = 4 against 57.4 at 2; 4-byte ones 57.4 us at 8 against 59.6
+// at 4).  With both halves in one thread 16-bit rows want 4 for 16-byte
+// accesses ([0, 48): 45.2 us against 49.4 at 2) and 2 otherwise, except the
+// positions call, which wants 2 (gqa 44.8 us against 47.4 at 4).  The
+// element path is best at 8 (4 with both halves in one thread).
+int heads_cap(int e, int vec, int path, bool pair, bool lanes, bool pos) {
+    if (path == kScalarPair) return pair ? 4 : 8;
     if (e == 4) {
-        if (half) return 1;
-        return vec == 16 ? 1 : 2;
+        const int per_head = pair ? 2 * vec : vec;  // bytes of x per head
+        return per_head >= 32 ? 1 : 32 / per_head;
     }
-    if (half) return vec == 16 ? 4 : 2;
+    if (pair) return (vec == 16 && !pos) ? 4 : 2;
+    if (lanes) return vec == 16 ? 4 : (vec == 8 ? 4 : 8);
     return vec == 8 ? 2 : 4;
 }
 
@@ -224,15 +232,21 @@ rope_status_t make_plan(int dir, int mode, int dtype, const Seg* seg, int nseg, 
     // Host buffers (the *_host calls) are read across the host link, where
     // one head per thread ran fastest: gqa 0.81 ms against 1.05 ms with 4;
     // the large fp32 shape is link-bound at any value.
-    P->U = choose_heads_per_thread(N, host ? 1 : heads_cap(half && !P->lanes, e, P->vec, P->path));
-    // Grid: for 16-bit rows of one tensor (interleave, or half-split with the
-    // partner in another lane) a grid that covers the work once ran faster
-    // than a resident grid that strides over it (gqa 42.0 vs 44.7 us, 8- and
-    // 4-byte chunks 55-57 vs 61-62 us; half-split gqa 43.4 vs 44.2 us); fp32
-    // rows, the half-split kernel that holds both halves and the fused
-    // query + key call (22.5 vs 20.5 us) ran faster with the resident grid
-    // (fp32 8-byte chunks 103 vs 113 us, 16-byte chunks 87 vs 100 us).
-    P->full_grid = e == 2 && (!half || P->lanes) && nseg == 1;
+    const bool pair = half && !P->lanes;
+    P->U = choose_heads_per_thread(N, host ? 1 : heads_cap(e, P->vec, P->path, pair, P->lanes, pos));
+    // Grid: for one tensor, a grid of one block per 256 work items, whose
+    // blocks the hardware replaces as they finish, ran faster than a
+    // resident grid whose threads stride over the work (the large fp32
+    // shape 99.5 against 103.2 us, its positions call 97.1 against 103.9 us,
+    // [32, 96) 82.7 against 86.9 us; gqa 42.0 against 44.7 us; the 16-bit
+    // element path in half-split mode 75.8 against 83.8 us).  The exceptions
+    // ran faster on the resident grid: the fused query + key call (20.5
+    // against 22.5 us), fp32 rows read over the host link, and the table
+    // call's half-split kernel with both halves in one thread when an access
+    // holds more than two elements ([0, 96) fp32: 144 against 150 us; [0, 48)
+    // fp16: 45.2 against 47.4 us; [4, 52) fp16: 40.2 against 41.3 us).
+    const bool wide_pair = pair && !pos && P->path == kVector && P->vec / e > 2;
+    P->full_grid = nseg == 1 && (e == 2 || !host) && !wide_pair;
     const int64_t H = (N + P->U - 1) / P->U;
     if (H * P->C > int64_t(kMaxPieceTasks))
         return fail(ROPE_ERR_INVALID, "N=%lld heads with a %lld-lane slice exceed the per-token work "

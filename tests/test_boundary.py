@@ -162,11 +162,12 @@ def test_plans_of_the_named_workloads(lib):
     assert (p.path, p.vec_bytes, p.chunks_per_row, p.heads_per_thread) == (1, 16, 8, 4)
     # large fp32 with the slice at byte 136: 8-byte accesses hold whole pairs
     p = plan(lib, dtype=FP32, shape=(4, 8192, 32, 128), start=34, end=98, r_shape=(4, 8192, 1, 64))
-    assert (p.path, p.vec_bytes, p.chunks_per_row, p.heads_per_thread) == (1, 8, 32, 2)
-    assert p.blocks == 152 * 8  # fp32: a resident grid that strides over the work
-    # tiny fp32 and the small-model bf16 full-row slice
+    assert (p.path, p.vec_bytes, p.chunks_per_row, p.heads_per_thread) == (1, 8, 32, 4)
+    assert p.blocks == p.tasks // 256  # one block per 256 work items
+    # tiny fp32 (16-byte accesses: 2 heads per thread) and the small-model
+    # bf16 full-row slice
     p = plan(lib, dtype=FP32, shape=(1, 16, 2, 64), start=0, end=32, r_shape=(1, 16, 1, 32))
-    assert (p.path, p.vec_bytes, p.heads_per_thread, p.blocks) == (1, 16, 1, 1)
+    assert (p.path, p.vec_bytes, p.heads_per_thread, p.blocks) == (1, 16, 2, 1)
     p = plan(lib, dtype=BF16, shape=(16, 256, 12, 64), start=0, end=64, r_shape=(1, 256, 1, 64))
     assert (p.path, p.vec_bytes, p.heads_per_thread) == (1, 16, 4)
 
@@ -194,6 +195,23 @@ def test_heads_per_thread(lib, N, vec, U):
     start = 0 if vec == 16 else 4  # 8-byte slice offset forces 8-byte accesses for fp16
     p = plan(lib, shape=(1, 2, N, 24), start=start, end=start + 8, r_shape=(1, 2, 1, 8))
     assert p.vec_bytes == vec and p.heads_per_thread == U
+
+
+@pytest.mark.parametrize("start,end,mode,vec,U", [
+    (32, 96, 1, 16, 2),    # fp32 16-byte accesses: 32 bytes of x per thread
+    (34, 98, 1, 8, 4),     # 8-byte accesses
+    (1, 65, 1, 8, 8),      # odd start: the element path
+    (34, 98, 2, 8, 4),     # half-split, partner in another lane (32 accesses per row)
+    (0, 96, 2, 16, 1),     # half-split, 48 lanes per half = 12 accesses: both halves in one thread
+    (2, 98, 2, 8, 2),      # 24 accesses per half of 8 bytes: both halves in one thread
+])
+def test_heads_per_thread_fp32(lib, start, end, mode, vec, U):
+    """fp32 rows: about 32 bytes of x per thread (a thread that holds both
+    halves of a half-split pair counts both accesses)."""
+    st, p = plan_mode(lib, mode, dtype=FP32, shape=(4, 64, 32, 128), start=start, end=end,
+                      r_shape=(4, 64, 1, end - start))
+    assert st == OK and (p.vec_bytes, p.heads_per_thread) == (vec, U)
+    assert p.blocks == -(-p.tasks // 256)  # one block per 256 work items
 
 
 def test_huge_calls_split_into_launches(lib):
@@ -294,8 +312,8 @@ def test_half_split_plans(lib):
     # fp32 slice at byte 136: 8-byte accesses (each half is 128 bytes), 32 per row
     st, p = plan_mode(lib, HALF, dtype=FP32, shape=(4, 8192, 32, 128), start=34, end=98,
                       r_shape=(4, 8192, 1, 64))
-    assert st == OK and (p.path, p.vec_bytes, p.chunks_per_row, p.heads_per_thread) == (LANES, 8, 32, 2)
-    assert p.blocks == 152 * 8   # fp32 rows: the resident grid
+    assert st == OK and (p.path, p.vec_bytes, p.chunks_per_row, p.heads_per_thread) == (LANES, 8, 32, 4)
+    assert p.blocks == p.tasks // 256
     # fp16 odd start: single elements, both halves in one thread
     st, p = plan_mode(lib, HALF, start=1, end=9)
     assert st == OK and (p.path, p.vec_bytes, p.chunks_per_row) == (2, 2, 4)
@@ -312,6 +330,16 @@ def test_half_split_plans(lib):
     # 64 accesses of the first half
     st, p = plan_mode(lib, HALF, dtype=FP32, shape=(2, 4, 3, 512), start=0, end=512)
     assert st == OK and (p.path, p.vec_bytes, p.chunks_per_row) == (1, 16, 64)
+    # both halves in one thread with accesses of more than two elements:
+    # the resident grid (8 blocks per SM on 152 SMs); of two or fewer, one
+    # block per 256 work items
+    st, p = plan_mode(lib, HALF, dtype=FP32, shape=(4, 8192, 32, 128), start=0, end=96,
+                      r_shape=(4, 8192, 1, 96))
+    assert st == OK and (p.path, p.vec_bytes, p.heads_per_thread, p.blocks) == (1, 16, 1, 152 * 8)
+    st, p = plan_mode(lib, HALF, dtype=FP32, shape=(4, 8192, 32, 128), start=2, end=98,
+                      r_shape=(4, 8192, 1, 96))
+    assert st == OK and (p.path, p.vec_bytes, p.heads_per_thread) == (1, 8, 2)
+    assert p.blocks == p.tasks // 256
     # 32 accesses per row: the largest that fits one warp
     st, p = plan_mode(lib, HALF, dtype=FP32, shape=(2, 4, 3, 128), start=0, end=128)
     assert st == OK and (p.path, p.vec_bytes, p.chunks_per_row) == (LANES, 16, 32)
