@@ -230,8 +230,9 @@ rope_status_t make_plan(int dir, int mode, int dtype, const Seg* seg, int nseg, 
     if (P->lanes) P->C = static_cast<int>(C_row);
     P->r_head = R.rb[0][2] != 0 || R.rb[1][2] != 0;
     // Host buffers (the *_host calls) are read across the host link, where
-    // one head per thread ran fastest: gqa 0.81 ms against 1.05 ms with 4;
-    // the large fp32 shape is link-bound at any value.
+    // one head per thread ran fastest: gqa 0.81 ms against 0.87 ms with 4
+    // (1.05 ms on the full grid), mla_decode_q 0.42 against 0.45 ms; the
+    // large fp32 shape 2.18 ms against 2.26-2.30 ms with 2 or 4.
     const bool pair = half && !P->lanes;
     P->U = choose_heads_per_thread(N, host ? 1 : heads_cap(e, P->vec, P->path, pair, P->lanes, pos));
     // Grid: for one tensor, a grid of one block per 256 work items, whose
@@ -241,12 +242,14 @@ rope_status_t make_plan(int dir, int mode, int dtype, const Seg* seg, int nseg, 
     // [32, 96) 82.7 against 86.9 us; gqa 42.0 against 44.7 us; the 16-bit
     // element path in half-split mode 75.8 against 83.8 us).  The exceptions
     // ran faster on the resident grid: the fused query + key call (20.5
-    // against 22.5 us), fp32 rows read over the host link, and the table
+    // against 22.5 us), 16-bit rows read over the host link (mla_decode_q
+    // 422 against 441 us; gqa level at 815-819 us, while the large fp32
+    // shape there ran 2184 against 2291 us on the full grid), and the table
     // call's half-split kernel with both halves in one thread when an access
     // holds more than two elements ([0, 96) fp32: 144 against 150 us; [0, 48)
     // fp16: 45.2 against 47.4 us; [4, 52) fp16: 40.2 against 41.3 us).
     const bool wide_pair = pair && !pos && P->path == kVector && P->vec / e > 2;
-    P->full_grid = nseg == 1 && (e == 2 || !host) && !wide_pair;
+    P->full_grid = nseg == 1 && (host ? e == 4 : !wide_pair);
     const int64_t H = (N + P->U - 1) / P->U;
     if (H * P->C > int64_t(kMaxPieceTasks))
         return fail(ROPE_ERR_INVALID, "N=%lld heads with a %lld-lane slice exceed the per-token work "
