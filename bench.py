@@ -56,14 +56,39 @@ PROFILES = os.path.join(ROOT, "profiles")
 # small utilities
 # --------------------------------------------------------------------------
 
+def strip_c_comments(text: str) -> str:
+    """C/C++ source without its comments and with whitespace runs collapsed
+    (string and character literals kept as they are)."""
+    out, i, n = [], 0, len(text)
+    while i < n:
+        ch = text[i]
+        if ch in "\"'":
+            j = i + 1
+            while j < n and text[j] != ch:
+                j += 2 if text[j] == "\\" else 1
+            out.append(text[i:j + 1])
+            i = j + 1
+        elif text.startswith("//", i):
+            j = text.find("\n", i)
+            i = n if j < 0 else j
+        elif text.startswith("/*", i):
+            j = text.find("*/", i + 2)
+            i = n if j < 0 else j + 2
+            out.append(" ")
+        else:
+            out.append(ch)
+            i += 1
+    return " ".join("".join(out).split())
+
+
 def kernel_source_hash() -> str:
-    """Hash of the kernel sources, to tell whether stored ncu counters still
-    describe the kernel that runs."""
+    """Hash of the kernel sources with comments and layout removed, to tell
+    whether stored ncu counters still describe the code that runs."""
     h = hashlib.sha256()
     for f in sorted(os.listdir(CSRC)):
         if f.endswith((".cu", ".cuh", ".h", ".cpp")):
-            with open(os.path.join(CSRC, f), "rb") as fh:
-                h.update(f.encode() + b"\0" + fh.read())
+            with open(os.path.join(CSRC, f), encoding="utf-8") as fh:
+                h.update(f.encode() + b"\0" + strip_c_comments(fh.read()).encode())
     return h.hexdigest()[:16]
 
 

@@ -26,7 +26,9 @@
 //     so the pair swap happens inside a thread's registers (no shuffles);
 //     rows whose slice is not aligned for that fall back to a scalar path
 //     with one access per element ("scalar pair"); in half-split mode a
-//     chunk of the slice's first half is paired with the chunk L/2 lanes on;
+//     chunk's partner lies L/2 lanes on: in another lane of the warp when
+//     the row's chunks fit one warp (a shuffle brings it), otherwise in the
+//     same thread;
 //   * a thread keeps the chunk's cos/sin in registers and walks U
 //     consecutive heads of the same token (heads hg*U .. hg*U + U - 1),
 //     issuing all U loads of x before any arithmetic, so U accesses per
@@ -34,9 +36,10 @@
 //   * consecutive threads take consecutive chunks of a row, so a warp reads
 //     whole 32-byte sectors of each row's slice;
 //   * the flat work index is split by three multiply-high divisions per
-//     item; the grid either covers it once (16-bit interleave) or is sized to
-//     the resident blocks of all SMs and strides over it (the host picks the
-//     faster, measured per access kind).
+//     item; the grid usually covers it once (one block per 256 items, so
+//     the hardware starts a block as each one ends), and for the cases that
+//     measured faster that way it is sized to the resident blocks of all
+//     SMs and strides over the work (the host picks per access kind).
 // Only slice bytes are read or written; every other byte of x is untouched.
 #pragma once
 #include <cuda_bf16.h>
