@@ -29,9 +29,9 @@
  * deterministic: no atomics, no reductions.
  *
  * Memory: every pointer is a device pointer (or managed memory) on the
- * current CUDA device; the *_host entry points below take host buffers.  The caller owns every buffer; the library allocates
- * nothing and needs no workspace.  Calls are asynchronous on `stream` and
- * never synchronise.
+ * current CUDA device; the *_host entry points below take host buffers.
+ * The caller owns every buffer; the library allocates nothing and needs no
+ * workspace.  Calls are asynchronous on `stream` and never synchronise.
  *
  * Error behaviour: arguments are validated on the host before anything is
  * launched; an invalid call changes nothing and returns an error status.
