@@ -867,6 +867,11 @@ def main():
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "native":
         args.warmup = 3
+    world = dist_env()[0]
+    if args.gpus != world:
+        print(f"bench.py: --gpus {args.gpus} but {world} rank(s) were launched (N > 1 runs under "
+              f"torch.distributed.run with one rank per GPU); reporting the {world} that run",
+              file=sys.stderr)
     if args.impl == "reference":
         return reference_arm(args)
     return gpu_arm(args)
