@@ -536,7 +536,7 @@ def breakdown(device, peak):
             entry[d] = e
         out[name] = entry
         del xd, gd, c, s
-    out["mla_decode_qk"] = qk_breakdown(device, peak, flush)
+    out["fused_qk"] = qk_breakdown(device, peak, flush)
     out["half_split"] = half_breakdown(device, peak, flush, l2)
     out["positions"] = positions_breakdown(device, peak, flush, l2)
     torch.cuda.empty_cache()
@@ -621,11 +621,38 @@ def qk_breakdown(device, peak, flush):
     tf = time_launches(fused, 50, flush)
     ts = time_launches(separate, 50, flush)
     nbytes = synth.qk_algorithmic_bytes()
-    return {"fwd": {"fused_cold_us": round(tf * 1e6, 2), "separate_cold_us": round(ts * 1e6, 2),
-                    "fused_GB/s": round(nbytes / tf / 1e9, 1),
-                    "fused_frac": round(nbytes / tf / 1e9 / peak, 4),
-                    "what": "query (4096,1,128,192) [0,64) + key (4096,1,1,64) [0,64), bf16, one "
-                            "cos/sin row per token: one fused launch vs query then key"}}
+    out = {"fwd": {"fused_cold_us": round(tf * 1e6, 2), "separate_cold_us": round(ts * 1e6, 2),
+                   "fused_GB/s": round(nbytes / tf / 1e9, 1),
+                   "fused_frac": round(nbytes / tf / 1e9 / peak, 4),
+                   "what": "query (4096,1,128,192) [0,64) + key (4096,1,1,64) [0,64), bf16, one "
+                           "cos/sin row per token: one fused launch vs query then key"}}
+    del qd, kd, fused, one_q, one_k
+
+    # a GQA pair: the gqa query with 4 key heads of the same rows
+    g = synth.WORKLOADS["gqa"]
+    q = synth.normal(g.shape, g.dtype, g.seed)
+    k = synth.normal(g.shape[:2] + (4,) + g.shape[3:], g.dtype, g.seed + 600)
+    r1, r2 = synth.rope_table(synth.positions(g), g.L, g.dtype)
+    qd, kd = synth.to_torch(q, g.dtype).to(device), synth.to_torch(k, g.dtype).to(device)
+    c, s = synth.to_torch(r1, g.dtype).to(device), synth.to_torch(r2, g.dtype).to(device)
+    fused = binding.PreparedQK("fwd", qd, kd, c, s, (g.start, g.end), (g.start, g.end))
+    one_q = binding.prepare_fwd(qd, c, s, g.start, g.end)
+    one_k = binding.prepare_fwd(kd, c, s, g.start, g.end)
+    for _ in range(3):
+        fused()
+        separate()
+    tf = time_launches(fused, 50, flush)
+    ts = time_launches(separate, 50, flush)
+    tfb, tsb = time_back_to_back(fused, 50), time_back_to_back(separate, 25)
+    e = synth.ELEM_BYTES[g.dtype]
+    nbytes = 2 * (qd.numel() + kd.numel()) // g.shape[3] * g.L * e + 2 * r1.size * e
+    out["gqa_fwd"] = {"fused_cold_us": round(tf * 1e6, 2), "separate_cold_us": round(ts * 1e6, 2),
+                      "fused_steady_us": round(tfb * 1e6, 2), "separate_steady_us": round(tsb * 1e6, 2),
+                      "fused_frac": round(nbytes / tf / 1e9 / peak, 4),
+                      "fused_steady_frac": round(nbytes / tfb / 1e9 / peak, 4),
+                      "what": "query (32,2048,16,128) + key (32,2048,4,128), slices [0,64), fp16, "
+                              "cos/sin (1,2048,1,64): one fused launch vs query then key"}
+    return out
 
 
 def gpu_arm(args):
