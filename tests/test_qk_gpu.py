@@ -37,6 +37,19 @@ def test_mla_decode_query_and_key_full_size(direction):
     check(direction, a, b, r1, r2, "bf16", synth.QK_KEY_SLICE, synth.QK_KEY_SLICE, "mla")
 
 
+@pytest.mark.parametrize("direction", ["fwd", "bwd"])
+def test_gqa_query_and_key_full_size(direction):
+    """The GQA pair the benchmark times: the gqa query (32,2048,16,128) and
+    4 key heads of the same rows, slices [0, 64), fp16, one cos/sin row per
+    position shared by every batch; every element."""
+    g = synth.WORKLOADS["gqa"]
+    seed = g.seed + (0 if direction == "fwd" else 500)
+    q = synth.normal(g.shape, g.dtype, seed)
+    k = synth.normal(g.shape[:2] + (4,) + g.shape[3:], g.dtype, g.seed + 600)
+    r1, r2 = synth.rope_table(synth.positions(g), g.L, g.dtype)
+    check(direction, q, k, r1, r2, g.dtype, (g.start, g.end), (g.start, g.end), "gqa")
+
+
 CASES = [
     # (B, S), (Nq, Dq, qs, qe), (Nk, Dk, ks, ke), broadcast of cos/sin over (B, S)
     ((2, 5), (3, 64, 0, 32), (2, 48, 16, 48), (1, 1)),
