@@ -689,33 +689,48 @@ def gpu_arm(args):
         for call in calls:
             call()
     K = args.steps
-    ev = [torch.cuda.Event(enable_timing=True) for _ in range(nl * K + 1)]
+    # The timed region holds the K steps and nothing else: an event at each
+    # end.  Launches carry programmatic dependent launch, so each one's
+    # launch and ramp overlap the previous one's tail; an event between two
+    # launches would serialise them and add its own ~1.7 us.
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     sampler = ClockSampler(local)
     barrier(world)
     torch.cuda.synchronize(device)
     sampler.start()
-    ev[0].record(stream)
-    for i in range(K):
-        for j, call in enumerate(calls):
+    t0.record(stream)
+    for _ in range(K):
+        for call in calls:
             call()
-            ev[nl * i + j + 1].record(stream)
+    t1.record(stream)
     torch.cuda.synchronize(device)
     clocks = sampler.stop()
     barrier(world)
 
-    elapsed = ev[0].elapsed_time(ev[nl * K]) / 1e3
-    per_dir = [[ev[nl * i + j].elapsed_time(ev[nl * i + j + 1]) / 1e3 for i in range(K)]
-               for j in range(nl)]
+    elapsed = t0.elapsed_time(t1) / 1e3
     per_launch = w.algorithmic_bytes()
     bytes_step = nl * per_launch
     max_elapsed, total_bytes = reduce_timing(elapsed, bytes_step * K, world, device)
     value = total_bytes / max_elapsed / 1e9
 
-    # the dominant kernel: the direction with the larger share of the time
-    dom = max(range(nl), key=lambda j: sum(per_dir[j]))
-    times = per_dir[dom]
+    # Each direction timed alone, between its own events, after the timed
+    # region (these serialise the launches); the slower one names the
+    # dominant kernel, whose average launch duration over the timed region
+    # is the region's elapsed time over its launches (the step is nothing
+    # but these launches, back to back).
+    Ki = min(K, 50)
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(2 * nl * Ki)]
+    for i in range(Ki):
+        for j, call in enumerate(calls):
+            ev[2 * (nl * i + j)].record(stream)
+            call()
+            ev[2 * (nl * i + j) + 1].record(stream)
+    torch.cuda.synchronize(device)
+    isolated = [statistics.mean(ev[2 * (nl * i + j)].elapsed_time(ev[2 * (nl * i + j) + 1]) / 1e3
+                                for i in range(Ki)) for j in range(nl)]
+    dom = max(range(nl), key=lambda j: isolated[j])
     kname = kernel_name(plan, w.dtype, dom)
-    avg = sum(times) / len(times)
+    avg = elapsed / (nl * K)
     achieved = per_launch / avg / 1e9
     traffic = stored_traffic(kname, w.name)
     roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
@@ -723,8 +738,11 @@ def gpu_arm(args):
                 "peak_source": f"{peak_kind} (HBM copy bandwidth, MEASURED_PEAKS.json hbm_gbs)"
                 if peak_kind == "measured" else "fallback 6.8 TB/s",
                 "kernel": kname, "kernel_avg_us": round(avg * 1e6, 2),
-                "fwd_avg_us": round(1e6 * sum(per_dir[0]) / K, 2),
-                "bwd_avg_us": round(1e6 * sum(per_dir[1]) / K, 2) if nl > 1 else None,
+                "timing": "average launch duration over the timed region: its elapsed time "
+                          "(CUDA events at its two ends) over its launches, which are only this "
+                          "workload's forward and backward kernels back to back",
+                "isolated_avg_us": {d: round(isolated[j] * 1e6, 2)
+                                    for j, d in enumerate(w.directions)},
                 "algorithmic_bytes_per_launch": per_launch,
                 "traffic_note": "dram bytes read + written per launch, from the committed ncu "
                                 "summary of the same kernel sources (cold L2; part of the writes "

@@ -51,6 +51,21 @@
 
 namespace rope {
 
+// Programmatic dependent launch.  Every launch carries the programmatic
+// stream-serialisation attribute, so the next kernel in the stream may start
+// before this one has finished.  Each block first lets the next grid launch
+// (it launches once every block of this grid has started, so its blocks
+// never take the slots of blocks of ours that still wait to run), then
+// waits until the grids it depends on have completed and their writes are
+// visible.  No global memory is touched before that wait, so a call behaves
+// exactly as if fully serialised after whatever the stream ran before it; what
+// overlaps is only the launch and ramp of one grid with the tail of the
+// previous one.  Without a programmatic predecessor the wait returns at once.
+__device__ __forceinline__ void enter_after_predecessor() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
 template <int W>
 struct Words {
     uint32_t w[W];
@@ -382,6 +397,7 @@ __device__ __forceinline__ void rope_body(const KernelArgs& a) {
     const char* const __restrict__ r2base = a.r2;
     const uint64_t stride = uint64_t(gridDim.x) * kThreads;
 
+    enter_after_predecessor();
     for (uint64_t t = uint64_t(blockIdx.x) * kThreads + threadIdx.x; t < a.tasks; t += stride) {
         uint32_t rest, c, tok, hg, b, s;
         a.divC.divmod(uint32_t(t), rest, c);
@@ -556,6 +572,7 @@ __global__ void __launch_bounds__(kThreads) rope_partial_half_lanes_kernel(const
     const uint32_t lane = threadIdx.x & 31u;
     const uint64_t stride = uint64_t(gridDim.x) * kThreads;
 
+    enter_after_predecessor();
     for (uint64_t t = uint64_t(blockIdx.x) * kThreads + threadIdx.x; t < a.tasks; t += stride) {
         // the lanes of this warp still in the loop: items t - lane .. tasks - 1
         // (tasks is a multiple of C, so a lane's partner is always among them)
@@ -714,6 +731,7 @@ rope_partial_pos_kernel(const KernelArgs a, const FreqTable f) {
     constexpr int NA = HALF ? E : (E / 2 > 0 ? E / 2 : 1);
     const uint64_t stride = uint64_t(gridDim.x) * kThreads;
 
+    enter_after_predecessor();
     for (uint64_t t = uint64_t(blockIdx.x) * kThreads + threadIdx.x; t < a.tasks; t += stride) {
         uint32_t rest, c, tok, hg, b, s;
         a.divC.divmod(uint32_t(t), rest, c);

@@ -145,8 +145,20 @@ rope_status_t launch_piece(const Plan& plan, const KernelArgs& args, const FreqT
     KernelArgs a = args;
     // rope_partial_pos_kernel takes the frequency table as a second parameter
     void* params[] = {&a, const_cast<FreqTable*>(freq)};
-    const cudaError_t e = cudaLaunchKernel(f, dim3(blocks), dim3(kThreads), params, 0,
-                                           reinterpret_cast<cudaStream_t>(stream));
+    // programmatic dependent launch: the kernels wait (griddepcontrol.wait)
+    // before their first global access, so the next launch may overlap the
+    // tail of this one
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(blocks);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = reinterpret_cast<cudaStream_t>(stream);
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    const cudaError_t e = cudaLaunchKernelExC(&cfg, f, params);
     if (e != cudaSuccess) return cuda_fail(e, err);
     return ROPE_OK;
 }
