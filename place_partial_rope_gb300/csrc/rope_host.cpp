@@ -234,27 +234,33 @@ rope_status_t make_plan(int dir, int mode, int dtype, const Seg* seg, int nseg, 
     // (1.05 ms on the full grid), mla_decode_q 0.42 against 0.45 ms; the
     // large fp32 shape 2.18 ms against 2.26-2.30 ms with 2 or 4.
     const bool pair = half && !P->lanes;
-    P->U = choose_heads_per_thread(N, host ? 1 : heads_cap(e, P->vec, P->path, pair, P->lanes, pos));
+    P->U = choose_heads_per_thread(seg[0].N,
+                                   host ? 1 : heads_cap(e, P->vec, P->path, pair, P->lanes, pos));
     // Grid: for one tensor, a grid of one block per 256 work items, whose
     // blocks the hardware replaces as they finish, ran faster than a
     // resident grid whose threads stride over the work (the large fp32
     // shape 99.5 against 103.2 us, its positions call 97.1 against 103.9 us,
     // [32, 96) 82.7 against 86.9 us; gqa 42.0 against 44.7 us; the 16-bit
-    // element path in half-split mode 75.8 against 83.8 us).  The exceptions
-    // ran faster on the resident grid: the fused query + key call (20.5
-    // against 22.5 us), 16-bit rows read over the host link (mla_decode_q
+    // element path in half-split mode 75.8 against 83.8 us; the fused query
+    // + key call, whose work index sweeps the query, then the key, 47.3
+    // against 51.2 us cold on a GQA pair).  The exceptions ran faster on the
+    // resident grid: 16-bit rows read over the host link (mla_decode_q
     // 422 against 441 us; gqa level at 815-819 us, while the large fp32
     // shape there ran 2184 against 2291 us on the full grid), and the table
     // call's half-split kernel with both halves in one thread when an access
     // holds more than two elements ([0, 96) fp32: 144 against 150 us; [0, 48)
     // fp16: 45.2 against 47.4 us; [4, 52) fp16: 40.2 against 41.3 us).
     const bool wide_pair = pair && !pos && P->path == kVector && P->vec / e > 2;
-    P->full_grid = nseg == 1 && (host ? e == 4 : !wide_pair);
-    const int64_t H = (N + P->U - 1) / P->U;
-    if (H * P->C > int64_t(kMaxPieceTasks))
+    P->full_grid = host ? (e == 4 && nseg == 1) : !wide_pair;
+    // head groups of each tensor (the fused call sweeps the first tensor's
+    // items, then the second's)
+    const int64_t H = (seg[0].N + P->U - 1) / P->U;
+    const int64_t H2 = nseg == 2 ? (seg[1].N + P->U - 1) / P->U : 0;
+    if ((H + H2) * P->C > int64_t(kMaxPieceTasks))
         return fail(ROPE_ERR_INVALID, "N=%lld heads with a %lld-lane slice exceed the per-token work "
                     "limit of 2^31 accesses", (long long)N, (long long)R.L);
     P->H = static_cast<int>(H);
+    P->H2 = static_cast<int>(H2);
     return ROPE_OK;
 }
 
@@ -284,6 +290,7 @@ KernelArgs base_args(const Plan& P, const Seg* seg, int nseg, const void* r1, co
     k.half_off = P.half ? (R.L / 2) * R.e : 0;
     k.divC = FastDiv::make(static_cast<uint32_t>(P.C));
     k.divH = FastDiv::make(static_cast<uint32_t>(P.H));
+    k.divH2 = FastDiv::make(static_cast<uint32_t>(P.H2 > 0 ? P.H2 : 1));
     return k;
 }
 
@@ -358,7 +365,7 @@ rope_status_t launch_all(int dir, int mode, int dtype, const Seg* seg, int nseg,
         whole.pos_s = pc_pos->pos_s;
         whole.pairs = static_cast<int32_t>(R.L / 2);
     }
-    const int64_t per_tok = int64_t(P.H) * P.C;
+    const int64_t per_tok = int64_t(P.H + P.H2) * P.C;
     return for_each_piece(B, S, per_tok, [&](const Piece& pc) -> rope_status_t {
         KernelArgs k = whole;
         const int64_t t0 = pc.b0 * S + pc.s0;
@@ -368,6 +375,7 @@ rope_status_t launch_all(int dir, int mode, int dtype, const Seg* seg, int nseg,
         if (k.r2) k.r2 += pc.b0 * whole.r2_b + pc.s0 * whole.r2_s;
         if (k.pos) k.pos += pc.b0 * whole.pos_b + pc.s0 * whole.pos_s;
         k.tasks = static_cast<uint32_t>(pc.count * per_tok);
+        k.tasks1 = static_cast<uint32_t>(pc.count * int64_t(P.H) * P.C);
         k.divS = FastDiv::make(static_cast<uint32_t>(pc.sp));
         const uint32_t blocks = static_cast<uint32_t>(grid_for(k.tasks, sms, bps, P.full_grid));
         const char* e2 = nullptr;
@@ -631,7 +639,7 @@ rope_status_t rope_partial_plan_mode(const void* x, const void* r1, const void* 
         if (device_sm_count(&sms, &err) != ROPE_OK) return fail(ROPE_ERR_CUDA, "%s", err);
         if (kernel_blocks_per_sm(P, &bps, &err) != ROPE_OK) return fail(ROPE_ERR_CUDA, "%s", err);
     }
-    const int64_t per_tok = int64_t(P.H) * P.C;
+    const int64_t per_tok = int64_t(P.H + P.H2) * P.C;
     int64_t max_blocks = 0, launches = 0;
     for_each_piece(B, S, per_tok, [&](const Piece& pc) -> rope_status_t {
         const int64_t g = grid_for(pc.count * per_tok, sms, bps, P.full_grid);

@@ -44,13 +44,16 @@ struct KernelArgs {
     const int32_t* pos;        // positions call: position of the piece's first (b, s)
     int64_t pos_b, pos_s;      // element strides of the positions (0: broadcast)
     int32_t pairs;             // positions call: L / 2 entries of the FreqTable
-    uint32_t tasks;            // work items of the piece: tokens * H * C
+    uint32_t tasks;            // work items of the piece: tokens * (H + H2) * C
+    uint32_t tasks1;           // fused query + key call: the first tensor's items
+                               // (tokens * H * C), which come before the second's
     int32_t N;                 // heads (first tensor's plus second tensor's)
     int32_t N1;                // heads of the first tensor
-    int32_t H;                 // head groups = ceil(N / U); group hg holds heads
-                               // hg*U .. hg*U + U - 1
+    int32_t H;                 // head groups of the first tensor = ceil(N1 / U);
+                               // group hg holds heads hg*U .. hg*U + U - 1
     FastDiv divC;              // chunks per row
-    FastDiv divH;              // head groups
+    FastDiv divH;              // head groups of the first tensor
+    FastDiv divH2;             // head groups of the second tensor (ceil((N - N1) / U))
     FastDiv divS;              // tokens per batch inside the piece
 };
 
@@ -61,7 +64,8 @@ struct Plan {
     int path;       // Path
     int vec;        // bytes per access of x: 16, 8 or 4 (vector), 2 * e (scalar pair)
     int U;          // heads per thread (cos/sin reused from registers across them)
-    int H;          // head groups
+    int H;          // head groups (of the first tensor when there are two)
+    int H2;         // head groups of the second tensor (0 when there is one)
     int C;          // chunks (accesses) per row slice
     bool r_head;    // cos/sin differ between heads: reloaded per head
     bool two;       // fused query + key call (rope_partial_qk_kernel)

@@ -374,21 +374,14 @@ __device__ __forceinline__ void rotate_half_chunks(const Words<W>& xa, const Wor
 //   T      storage type            VEC    bytes per access of x
 //   SCALAR element-wise accesses   U      heads per thread
 //   DIR    kFwd / kBwd             RHEAD  cos/sin differ between heads
-//   TWO    a second tensor's heads follow the first's (the fused query + key
-//          call): head n < N1 is row n of x, head n >= N1 is row n - N1 of x2;
-//          both use the token's one cos/sin row
+//   TWO    two tensors in one launch (the fused query + key call): the work
+//          items of the first (x, N1 heads, H head groups) come first, those
+//          of the second (x2, N - N1 heads, H2 head groups) after them, so
+//          each tensor is swept in address order as a launch of its own
+//          would; both use the token's one cos/sin row
 //   HALF   half-split mode: the chunk covers lanes of the slice's first half
 //          and pairs with the chunk half_off bytes further on (x and cos/sin)
 // ------------------------------------------------------------------------
-
-template <bool TWO>
-__device__ __forceinline__ char* head_row(const KernelArgs& a, uint32_t tok, int n) {
-    if constexpr (TWO) {
-        if (n >= a.N1)
-            return a.x2 + int64_t(tok) * a.tok_bytes2 + int64_t(n - a.N1) * a.row_bytes2;
-    }
-    return a.x + int64_t(tok) * a.tok_bytes + int64_t(n) * a.row_bytes;
-}
 
 template <typename T, int VEC, bool SCALAR, int U, int DIR, bool RHEAD, bool TWO, bool HALF>
 __device__ __forceinline__ void rope_body(const KernelArgs& a) {
@@ -399,22 +392,32 @@ __device__ __forceinline__ void rope_body(const KernelArgs& a) {
 
     enter_after_predecessor();
     for (uint64_t t = uint64_t(blockIdx.x) * kThreads + threadIdx.x; t < a.tasks; t += stride) {
-        uint32_t rest, c, tok, hg, b, s;
-        a.divC.divmod(uint32_t(t), rest, c);
-        a.divH.divmod(rest, tok, hg);
+        uint32_t task = uint32_t(t), rest, c, tok, hg, b, s;
+        char* xbase = a.x;
+        int64_t tok_bytes = a.tok_bytes, row_bytes = a.row_bytes;
+        int nheads = a.N;
+        FastDiv divH = a.divH;
+        if constexpr (TWO) {
+            const bool second = task >= a.tasks1;
+            if (second) task -= a.tasks1;
+            xbase = second ? a.x2 : a.x;
+            tok_bytes = second ? a.tok_bytes2 : a.tok_bytes;
+            row_bytes = second ? a.row_bytes2 : a.row_bytes;
+            nheads = second ? a.N - a.N1 : a.N1;
+            divH = second ? a.divH2 : a.divH;
+        }
+        a.divC.divmod(task, rest, c);
+        divH.divmod(rest, tok, hg);
         a.divS.divmod(tok, b, s);
 
         // this thread's heads are n0 .. n0 + U - 1 (consecutive rows)
         const int n0 = int(hg) * U;
         const int64_t c_off = int64_t(c) * VEC;
         char* xp[U];
-        if constexpr (TWO) {
+        {
+            char* x0 = xbase + int64_t(tok) * tok_bytes + int64_t(n0) * row_bytes + c_off;
 #pragma unroll
-            for (int i = 0; i < U; ++i) xp[i] = head_row<true>(a, tok, n0 + i) + c_off;
-        } else {
-            char* x0 = a.x + int64_t(tok) * a.tok_bytes + int64_t(n0) * a.row_bytes + c_off;
-#pragma unroll
-            for (int i = 0; i < U; ++i) xp[i] = x0 + i * a.row_bytes;
+            for (int i = 0; i < U; ++i) xp[i] = x0 + i * row_bytes;
         }
         const char* c_p = r1base + int64_t(b) * a.r1_b + int64_t(s) * a.r1_s + c_off;
         const char* s_p = r2base + int64_t(b) * a.r2_b + int64_t(s) * a.r2_s + c_off;
@@ -428,7 +431,7 @@ __device__ __forceinline__ void rope_body(const KernelArgs& a) {
             Words<W> xa[U], xb[U];
 #pragma unroll
             for (int i = 0; i < U; ++i)
-                if (i == 0 || n0 + i < a.N) {
+                if (i == 0 || n0 + i < nheads) {
                     xa[i] = load_x_half<T, W, SCALAR>(xp[i]);
                     xb[i] = load_x_half<T, W, SCALAR>(xp[i] + ho);
                 }
@@ -441,7 +444,7 @@ __device__ __forceinline__ void rope_body(const KernelArgs& a) {
             }
 #pragma unroll
             for (int i = 0; i < U; ++i) {
-                if (i == 0 || n0 + i < a.N) {
+                if (i == 0 || n0 + i < nheads) {
                     if constexpr (RHEAD) {
                         const int64_t o1 = int64_t(i) * a.r1_n, o2 = int64_t(i) * a.r2_n;
                         ca = load_r_half<T, W, SCALAR>(c_p + o1);
@@ -461,7 +464,7 @@ __device__ __forceinline__ void rope_body(const KernelArgs& a) {
         Words<W> xv[U];
 #pragma unroll
         for (int i = 0; i < U; ++i)
-            if (i == 0 || n0 + i < a.N) xv[i] = load_x<T, W, SCALAR>(xp[i]);
+            if (i == 0 || n0 + i < nheads) xv[i] = load_x<T, W, SCALAR>(xp[i]);
 
         Words<W> cv, sv;
         if constexpr (!RHEAD) {
@@ -470,7 +473,7 @@ __device__ __forceinline__ void rope_body(const KernelArgs& a) {
         }
 #pragma unroll
         for (int i = 0; i < U; ++i) {
-            if (i == 0 || n0 + i < a.N) {
+            if (i == 0 || n0 + i < nheads) {
                 if constexpr (RHEAD) {
                     cv = load_r<T, W, SCALAR>(c_p + int64_t(i) * a.r1_n);
                     sv = load_r<T, W, SCALAR>(s_p + int64_t(i) * a.r2_n);
