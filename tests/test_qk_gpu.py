@@ -83,3 +83,36 @@ def test_fused_equals_two_single_launches():
     torch.cuda.synchronize()
     assert torch.equal(qd.view(torch.int16), q2.view(torch.int16))
     assert torch.equal(kd.view(torch.int16), k2.view(torch.int16))
+
+
+def test_fused_call_split_into_several_launches():
+    """Query and key of one pair per row over 2^30 + 3 tokens each: 2^31 + 6
+    work items, so the fused call runs as two launches, each covering the
+    query's items of its tokens, then the key's.  With cos = 0 and sin = 1
+    the forward is the exact quarter turn (a, b) -> (-b, a) at any size; rows
+    at the start, at the launch boundary and at the end are also checked
+    against the oracle with a random table."""
+    S = 2**30 + 3
+    g = torch.Generator(device=DEV).manual_seed(4321)
+    q = torch.randn((1, S, 1, 2), generator=g, device=DEV, dtype=torch.float32).to(torch.float16)
+    k = torch.randn((1, S, 1, 4), generator=g, device=DEV, dtype=torch.float32).to(torch.float16)
+    zero = torch.zeros((1, 1, 1, 2), dtype=torch.float16, device=DEV)
+    one = torch.ones((1, 1, 1, 2), dtype=torch.float16, device=DEV)
+    q0, k0 = q.clone(), k.clone()
+    binding.rope_partial_inplace_fwd_qk(q, k, zero, one, (0, 2), (2, 4))
+    torch.cuda.synchronize()
+    assert torch.equal(q[..., 0], -q0[..., 1]) and torch.equal(q[..., 1], q0[..., 0])
+    assert torch.equal(k[..., 2], -k0[..., 3]) and torch.equal(k[..., 3], k0[..., 2])
+    assert torch.equal(k[..., :2], k0[..., :2])
+    c_h, s_h = synth.random_table((1, 1, 1, 2), "fp16", 19)
+    q2, k2 = q0.clone(), k0.clone()
+    binding.rope_partial_inplace_fwd_qk(q2, k2, to_dev(c_h, "fp16"), to_dev(s_h, "fp16"), (0, 2), (2, 4))
+    torch.cuda.synchronize()
+    for t0 in (0, 2**30 - 2, S - 3):
+        qi = synth.from_torch(q0[:, t0:t0 + 3])
+        ki = synth.from_torch(k0[:, t0:t0 + 3])
+        wq, wk = oracle.rope_qk(oracle.FWD, qi, ki, c_h, s_h, "fp16", (0, 2), (2, 4))
+        assert_same(synth.from_torch(q2[:, t0:t0 + 3]), wq, "fp16", f"query rows at {t0}")
+        assert_same(synth.from_torch(k2[:, t0:t0 + 3]), wk, "fp16", f"key rows at {t0}")
+    del q, k, q0, k0, q2, k2
+    torch.cuda.empty_cache()
