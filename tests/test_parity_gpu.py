@@ -62,6 +62,32 @@ def test_sweep(dtype, k):
         assert_same(got, want, dtype, f"{shape} [{st},{en}) {form} {direction}")
 
 
+ODD_STARTS = [
+    # 16-bit rows with an odd start (the element path): pair counts that are
+    # multiples of 4, of 2 and odd, idle head slots, the slice ending one
+    # element before the row's end, cos/sin per head, one pair per row
+    ((2, 5, 3, 64), 1, 63, "BS1D"),       # 31 pairs: 1 per access; ends at D - 1
+    ((2, 5, 3, 64), 3, 35, "B11D"),       # 16 pairs: 4 per access
+    ((2, 5, 6, 64), 5, 17, "1S1D"),       # 6 pairs: 2 per access; 6 heads, U = 4
+    ((2, 4, 5, 40), 7, 39, "BSND"),       # cos/sin per head
+    ((1, 3, 9, 8), 1, 7, "1SND"),         # 3 pairs, cos/sin per head
+    ((3, 2, 4, 4), 1, 3, "B1ND"),         # one pair per row
+    ((1, 7, 2, 1024), 1, 1023, "1S1D"),   # the longest odd slice
+    ((2, 3, 16, 128), 33, 97, "BS1D"),    # gqa-like rows, [33, 97)
+]
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "fp16"])
+@pytest.mark.parametrize("k", range(len(ODD_STARTS)))
+def test_odd_starts_16bit(dtype, k):
+    shape, st, en, form = ODD_STARTS[k]
+    x, r1, r2, g = synth.case(shape, st, en, dtype, form, seed=1500 + k)
+    for direction, inp in (("fwd", x), ("bwd", g)):
+        got = run_cuda(direction, inp, r1, r2, dtype, st, en)
+        want = run_oracle(direction, inp, r1, r2, dtype, st, en)
+        assert_same(got, want, dtype, f"{shape} [{st},{en}) {form} {direction}")
+
+
 @pytest.mark.parametrize("dtype", ["bf16", "fp16", "fp32"])
 @pytest.mark.parametrize("elem_offset", [0, 1, 2, 4])
 def test_guard_bands_and_misaligned_base(dtype, elem_offset):
