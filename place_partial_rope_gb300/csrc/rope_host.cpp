@@ -148,6 +148,7 @@ rope_status_t check(const void* x, const void* r1, const void* r2, int dtype, in
 // element path is best at 8 (4 with both halves in one thread).
 int heads_cap(int e, int vec, int path, bool pair, bool lanes, bool pos) {
     if (path == kScalarPair) return pair ? 4 : 8;
+    if (path == kOddPair) return vec;  // the caller passes the cap for this path
     if (e == 4) {
         const int per_head = pair ? 2 * vec : vec;  // bytes of x per head
         return per_head >= 32 ? 1 : 32 / per_head;
@@ -202,10 +203,24 @@ rope_status_t make_plan(int dir, int mode, int dtype, const Seg* seg, int nseg, 
     P->dir = dir;
     P->two = nseg == 2;
     P->half = half;
+    // 16-bit interleave with an odd start, rows of 1..32 pairs (a power of
+    // two): a lane per aligned word of x (the row pitch is a multiple of 4
+    // bytes since D is even; the element after the slice exists since end
+    // is odd and D even), cos/sin of pair p as their rows' aligned word p
+    const int64_t pairs = R.L / 2;
+    const bool odd = !vec && !half && !pos && nseg == 1 && e == 2 && (seg[0].start & 1) &&
+                     reinterpret_cast<uintptr_t>(seg[0].x) % 4 == 0 && pairs <= 32 &&
+                     (pairs & (pairs - 1)) == 0 && p1 % 4 == 0 && p2 % 4 == 0 &&
+                     R.rb[0][0] % 4 == 0 && R.rb[0][1] % 4 == 0 && R.rb[0][2] % 4 == 0 &&
+                     R.rb[1][0] % 4 == 0 && R.rb[1][1] % 4 == 0 && R.rb[1][2] % 4 == 0;
     if (vec) {
         P->path = kVector;
         P->vec = vec;
         P->C = static_cast<int>(Lb / vec);
+    } else if (odd) {
+        P->path = kOddPair;
+        P->vec = 4;
+        P->C = static_cast<int>(pairs);
     } else if (half) {
         P->path = kScalarPair;  // a 16-bit slice not aligned for 4-byte accesses
         P->vec = e;
@@ -234,8 +249,12 @@ rope_status_t make_plan(int dir, int mode, int dtype, const Seg* seg, int nseg, 
     // (1.05 ms on the full grid), mla_decode_q 0.42 against 0.45 ms; the
     // large fp32 shape 2.18 ms against 2.26-2.30 ms with 2 or 4.
     const bool pair = half && !P->lanes;
+    // the odd-start path: 8 heads per thread on rows of 16 or 32 pairs (gqa
+    // [1, 65): 69.8 us against 72.5 at 4 and 73.4 on the element path), 2 on
+    // shorter rows ([1, 17): 29.4 us against 30.1 at 4 and 33.3)
+    const int cap_vec = P->path == kOddPair ? (P->C >= 16 ? 8 : 2) : P->vec;
     P->U = choose_heads_per_thread(seg[0].N,
-                                   host ? 1 : heads_cap(e, P->vec, P->path, pair, P->lanes, pos));
+                                   host ? 1 : heads_cap(e, cap_vec, P->path, pair, P->lanes, pos));
     // Grid: for one tensor, a grid of one block per 256 work items, whose
     // blocks the hardware replaces as they finish, ran faster than a
     // resident grid whose threads stride over the work (the large fp32
@@ -647,7 +666,7 @@ rope_status_t rope_partial_plan_mode(const void* x, const void* r1, const void* 
         ++launches;
         return ROPE_OK;
     });
-    plan->path = P.lanes ? 3 : P.path;
+    plan->path = P.lanes ? 3 : P.path;  // kOddPair reports 4
     plan->vec_bytes = P.vec;
     plan->heads_per_thread = P.U;
     plan->threads_per_block = kThreads;

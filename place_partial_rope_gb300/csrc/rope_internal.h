@@ -22,7 +22,7 @@ struct FreqTable {
 };
 
 enum Direction : int { kFwd = 0, kBwd = 1 };
-enum Path : int { kNone = 0, kVector = 1, kScalarPair = 2 };
+enum Path : int { kNone = 0, kVector = 1, kScalarPair = 2, kOddPair = 4 };
 enum Mode : int { kInterleave = 1, kHalf = 2 };  // the ACLNN numbering: interleave = 1
 
 // What one launch covers: a contiguous range of tokens ("a piece").  The

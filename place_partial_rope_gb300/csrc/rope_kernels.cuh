@@ -6,6 +6,8 @@
 //                            warp: the partner access comes by warp shuffle
 //   rope_partial_qk_kernel   query and key in one launch, one cos/sin row
 //   rope_partial_pos_kernel  cos/sin computed from positions (no table)
+//   rope_partial_odd_kernel  16-bit interleave with an odd start: a lane
+//                            per aligned word, straddling halves by shuffle
 //
 // What it computes ("CANN ops-transformer inplace_partial_rotary_mul",
 // section 功能与计算公式, and its kernel op chain): for every row
@@ -503,6 +505,95 @@ __global__ void __launch_bounds__(kThreads) rope_partial_half_kernel(const Kerne
 }
 
 // ------------------------------------------------------------------------
+// 16-bit interleave mode with an odd start: pairs across aligned words
+// ------------------------------------------------------------------------
+// With an odd start, pair p of a row (elements start + 2p and start + 2p + 1)
+// straddles two aligned 4-byte words: the high half of word p and the low
+// half of word p + 1, counting words from the one that holds element
+// start - 1.  For rows of P pairs with P a power of two in [1, 32], lane p
+// of a row loads word p (a warp's loads are contiguous), takes the low half
+// of word p + 1 from lane p + 1 by shuffle (the row's last lane loads word P
+// itself) and stores word p whole: its low half is the previous pair's
+// second result, taken from lane p - 1 by shuffle.  The row's first lane
+// stores only the high half of word 0 and its last lane only the low half of
+// word P (2-byte stores), so no byte outside the slice is written.
+template <typename T, int U, int DIR, bool RHEAD>
+__global__ void __launch_bounds__(kThreads) rope_partial_odd_kernel(const KernelArgs a) {
+    static_assert(sizeof(T) == 2, "the odd-start path is for 16-bit storage");
+    using P = Pack<T>;
+    const uint32_t C = a.divC.d;  // pairs (= lanes) per row: a power of two in [1, 32]
+    const uint32_t lane = threadIdx.x & 31u;
+    const uint64_t stride = uint64_t(gridDim.x) * kThreads;
+    enter_after_predecessor();
+    for (uint64_t t = uint64_t(blockIdx.x) * kThreads + threadIdx.x; t < a.tasks; t += stride) {
+        // the lanes of this warp still in the loop (tasks is a multiple of C,
+        // so they hold whole rows)
+        const uint64_t left = a.tasks - (t - lane);
+        const uint32_t mask = left >= 32 ? 0xffffffffu : ((1u << uint32_t(left)) - 1u);
+        uint32_t rest, p, tok, hg, b, s;
+        a.divC.divmod(uint32_t(t), rest, p);
+        a.divH.divmod(rest, tok, hg);
+        a.divS.divmod(tok, b, s);
+        const bool first = p == 0, last = p + 1 == C;
+        const int n0 = int(hg) * U;
+        // word p of head n0's row: row elements start - 1 + 2p (low half)
+        // and start + 2p (high half)
+        char* w0 = a.x - 2 + int64_t(tok) * a.tok_bytes + int64_t(n0) * a.row_bytes + int64_t(p) * 4;
+        const char* c_p = a.r1 + int64_t(b) * a.r1_b + int64_t(s) * a.r1_s + int64_t(p) * 4;
+        const char* s_p = a.r2 + int64_t(b) * a.r2_b + int64_t(s) * a.r2_s + int64_t(p) * 4;
+        if constexpr (RHEAD) {
+            c_p += int64_t(n0) * a.r1_n;
+            s_p += int64_t(n0) * a.r2_n;
+        }
+
+        uint32_t xw[U], xn[U];  // word p, and word p + 1 for the row's last lane
+#pragma unroll
+        for (int i = 0; i < U; ++i) {
+            xw[i] = 0u;
+            xn[i] = 0u;
+            if (i == 0 || n0 + i < a.N) {
+                xw[i] = ld_vec<1>(w0 + i * a.row_bytes).w[0];
+                if (last) xn[i] = ld_vec<1>(w0 + i * a.row_bytes + 4).w[0];
+            }
+        }
+        uint32_t cw = 0u, sw = 0u;
+        if constexpr (!RHEAD) {
+            cw = ldg_vec<1>(c_p).w[0];
+            sw = ldg_vec<1>(s_p).w[0];
+        }
+#pragma unroll
+        for (int i = 0; i < U; ++i) {
+            // every lane of `mask` shuffles, outside any per-lane condition
+            const uint32_t down = __shfl_down_sync(mask, xw[i], 1);
+            const uint32_t nxt = last ? xn[i] : down;
+            if constexpr (RHEAD) {
+                if (i == 0 || n0 + i < a.N) {
+                    cw = ldg_vec<1>(c_p + int64_t(i) * a.r1_n).w[0];
+                    sw = ldg_vec<1>(s_p + int64_t(i) * a.r2_n).w[0];
+                }
+            }
+            float lo, x0, x1, hi, c0, c1, s0, s1, y0, y1;
+            P::get(&xw[i], lo, x0);  // x0: element start + 2p
+            P::get(&nxt, x1, hi);    // x1: element start + 2p + 1
+            P::get(&cw, c0, c1);
+            P::get(&sw, s0, s1);
+            rotate_pair<DIR>(x0, x1, c0, c1, s0, s1, y0, y1);
+            const uint32_t y0b = Elem<T>::put(y0), y1b = Elem<T>::put(y1);
+            const uint32_t prev = __shfl_up_sync(mask, y1b, 1);  // the previous pair's second result
+            if (i == 0 || n0 + i < a.N) {
+                char* wp = w0 + i * a.row_bytes;
+                if (first) {
+                    st_elem_scalar<T>(wp + 2, Words<1>{{y0b}});
+                } else {
+                    st_vec<1>(wp, Words<1>{{(prev & 0xffffu) | (y0b << 16)}});
+                }
+                if (last) st_elem_scalar<T>(wp + 4, Words<1>{{y1b}});
+            }
+        }
+    }
+}
+
+// ------------------------------------------------------------------------
 // half-split mode with the partner access in another lane
 // ------------------------------------------------------------------------
 // When a row's slice is C accesses long with C a power of two in [2, 32],
@@ -783,7 +874,7 @@ rope_partial_pos_kernel(const KernelArgs a, const FreqTable f) {
 // kernel selection for one storage type (instantiated in one .cu per type)
 // ------------------------------------------------------------------------
 
-enum Kind { kSingle, kQK, kHalfSplit, kHalfLanes, kPos, kPosHalf };
+enum Kind { kSingle, kQK, kHalfSplit, kHalfLanes, kPos, kPosHalf, kOdd };
 
 template <typename T, int VEC, bool SCALAR, int U, Kind K>
 const void* pick_dir(const Plan& p) {
@@ -792,6 +883,16 @@ const void* pick_dir(const Plan& p) {
         constexpr bool H = K == kPosHalf;
         return f ? reinterpret_cast<const void*>(&rope_partial_pos_kernel<T, VEC, SCALAR, U, kFwd, H>)
                  : reinterpret_cast<const void*>(&rope_partial_pos_kernel<T, VEC, SCALAR, U, kBwd, H>);
+    } else if constexpr (K == kOdd) {
+        if constexpr (sizeof(T) == 2) {
+            if (f)
+                return p.r_head ? reinterpret_cast<const void*>(&rope_partial_odd_kernel<T, U, kFwd, true>)
+                                : reinterpret_cast<const void*>(&rope_partial_odd_kernel<T, U, kFwd, false>);
+            return p.r_head ? reinterpret_cast<const void*>(&rope_partial_odd_kernel<T, U, kBwd, true>)
+                            : reinterpret_cast<const void*>(&rope_partial_odd_kernel<T, U, kBwd, false>);
+        } else {
+            return nullptr;
+        }
     } else if constexpr (K == kQK) {
         return f ? reinterpret_cast<const void*>(&rope_partial_qk_kernel<T, VEC, SCALAR, U, kFwd>)
                  : reinterpret_cast<const void*>(&rope_partial_qk_kernel<T, VEC, SCALAR, U, kBwd>);
@@ -873,6 +974,10 @@ const void* pick_half(const Plan& p) {
 
 template <typename T>
 const void* pick_kernel(const Plan& p) {
+    if (p.path == kOddPair) {
+        if constexpr (sizeof(T) == 2) return pick_heads<T, 4, false, kOdd>(p);
+        else return nullptr;
+    }
     if (p.pos) return p.half ? pick_half<T, kPosHalf>(p) : pick_interleave<T, kPos>(p);
     if (p.half) return p.lanes ? pick_half_lanes<T>(p) : pick_half<T, kHalfSplit>(p);
     if (p.two) return pick_interleave<T, kQK>(p);

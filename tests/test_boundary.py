@@ -173,8 +173,17 @@ def test_plans_of_the_named_workloads(lib):
 
 
 def test_path_choice(lib):
-    assert plan(lib, start=1, end=9).path == 2                       # odd start: scalar pairs
-    assert plan(lib, dtype=FP32, start=1, end=9).path == 2
+    ODD = 4
+    # 16-bit odd start, rows of 1..32 pairs (a power of two): a lane per aligned word
+    p = plan(lib, start=1, end=9)
+    assert (p.path, p.vec_bytes, p.chunks_per_row, p.heads_per_thread) == (ODD, 4, 4, 2)
+    p = plan(lib, dtype=FP16, shape=(32, 2048, 16, 128), start=1, end=65, r_shape=(1, 2048, 1, 64))
+    assert (p.path, p.chunks_per_row, p.heads_per_thread) == (ODD, 32, 8)
+    assert p.blocks == p.tasks // 256
+    assert plan(lib, shape=(2, 4, 3, 16), start=1, end=7, r_shape=(1, 4, 1, 6)).path == 2  # 3 pairs
+    assert plan(lib, start=1, end=9, x=BASE + 2).path == 2           # x only 2-byte aligned
+    assert plan(lib, start=1, end=9, r1=BASE + 2**30 + 2).path == 2  # cos only 2-byte aligned
+    assert plan(lib, dtype=FP32, start=1, end=9).path == 2          # fp32 odd start: scalar pairs
     assert plan(lib, start=2, end=10).vec_bytes == 4                 # 4-byte slice offset
     assert plan(lib, x=BASE + 8).vec_bytes == 8                      # x only 8-byte aligned
     assert plan(lib, r1=BASE + 2**30 + 4).vec_bytes == 4             # cos only 4-byte aligned

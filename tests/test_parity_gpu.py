@@ -63,25 +63,30 @@ def test_sweep(dtype, k):
 
 
 ODD_STARTS = [
-    # 16-bit rows with an odd start (the element path): pair counts that are
-    # multiples of 4, of 2 and odd, idle head slots, the slice ending one
-    # element before the row's end, cos/sin per head, one pair per row
-    ((2, 5, 3, 64), 1, 63, "BS1D"),       # 31 pairs: 1 per access; ends at D - 1
-    ((2, 5, 3, 64), 3, 35, "B11D"),       # 16 pairs: 4 per access
-    ((2, 5, 6, 64), 5, 17, "1S1D"),       # 6 pairs: 2 per access; 6 heads, U = 4
-    ((2, 4, 5, 40), 7, 39, "BSND"),       # cos/sin per head
-    ((1, 3, 9, 8), 1, 7, "1SND"),         # 3 pairs, cos/sin per head
-    ((3, 2, 4, 4), 1, 3, "B1ND"),         # one pair per row
-    ((1, 7, 2, 1024), 1, 1023, "1S1D"),   # the longest odd slice
-    ((2, 3, 16, 128), 33, 97, "BS1D"),    # gqa-like rows, [33, 97)
+    # 16-bit rows with an odd start: rows of 1..32 pairs (a power of two)
+    # run a lane per aligned word of x (path 4), the others the element
+    # path (path 2); idle head slots, the slice ending one element before
+    # the row's end, cos/sin per head, one pair per row
+    ((2, 5, 3, 64), 1, 63, "BS1D", 2),       # 31 pairs; ends at D - 1
+    ((2, 5, 3, 64), 3, 35, "B11D", 4),       # 16 pairs
+    ((2, 5, 6, 64), 5, 17, "1S1D", 2),       # 6 pairs; 6 heads
+    ((2, 4, 5, 40), 7, 39, "BSND", 4),       # 16 pairs, cos/sin per head
+    ((1, 3, 9, 8), 1, 7, "1SND", 2),         # 3 pairs, cos/sin per head
+    ((3, 2, 4, 4), 1, 3, "B1ND", 4),         # one pair per row, ends at D - 1
+    ((1, 7, 2, 1024), 1, 1023, "1S1D", 2),   # the longest odd slice
+    ((2, 3, 16, 128), 33, 97, "BS1D", 4),    # gqa-like rows, 32 pairs, U = 8
+    ((2, 3, 13, 66), 1, 65, "BS1D", 4),      # 13 heads (idle slots at U = 8)
+    ((1, 5, 6, 20), 3, 19, "BSND", 4),       # 8 pairs: 4 rows per warp
 ]
 
 
 @pytest.mark.parametrize("dtype", ["bf16", "fp16"])
 @pytest.mark.parametrize("k", range(len(ODD_STARTS)))
 def test_odd_starts_16bit(dtype, k):
-    shape, st, en, form = ODD_STARTS[k]
+    shape, st, en, form, path = ODD_STARTS[k]
     x, r1, r2, g = synth.case(shape, st, en, dtype, form, seed=1500 + k)
+    assert binding.rope_partial_plan(to_dev(x, dtype), to_dev(r1, dtype), to_dev(r2, dtype),
+                                     st, en).path == path
     for direction, inp in (("fwd", x), ("bwd", g)):
         got = run_cuda(direction, inp, r1, r2, dtype, st, en)
         want = run_oracle(direction, inp, r1, r2, dtype, st, en)
