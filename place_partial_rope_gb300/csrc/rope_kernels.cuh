@@ -30,7 +30,9 @@
 //     with one access per element ("scalar pair"); in half-split mode a
 //     chunk's partner lies L/2 lanes on: in another lane of the warp when
 //     the row's chunks fit one warp (a shuffle brings it), otherwise in the
-//     same thread;
+//     same thread; a 16-bit slice with an odd start has its pairs straddle
+//     aligned words, and rows of up to 32 pairs then take a lane per word
+//     with the straddling halves brought by shuffle;
 //   * a thread keeps the chunk's cos/sin in registers and walks U
 //     consecutive heads of the same token (heads hg*U .. hg*U + U - 1),
 //     issuing all U loads of x before any arithmetic, so U accesses per
@@ -41,7 +43,10 @@
 //     item; the grid usually covers it once (one block per 256 items, so
 //     the hardware starts a block as each one ends), and for the cases that
 //     measured faster that way it is sized to the resident blocks of all
-//     SMs and strides over the work (the host picks per access kind).
+//     SMs and strides over the work (the host picks per access kind);
+//   * launches use programmatic dependent launch: every kernel waits on
+//     griddepcontrol before its first global access, so only its launch and
+//     ramp overlap the tail of the kernel before it in the stream.
 // Only slice bytes are read or written; every other byte of x is untouched.
 #pragma once
 #include <cuda_bf16.h>
