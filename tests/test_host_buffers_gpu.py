@@ -38,7 +38,9 @@ def run_host(direction, x, r1, r2, dtype, start, end, pin=True, r_on_device=Fals
 @pytest.mark.parametrize("shape,st,en,form", [((2, 5, 3, 64), 0, 64, "BS1D"),
                                               ((2, 5, 3, 64), 34, 62, "BSND"),
                                               ((3, 7, 5, 40), 3, 37, "1S1D"),
-                                              ((1, 300, 4, 128), 0, 64, "1S1D")])
+                                              ((1, 300, 4, 128), 0, 64, "1S1D"),
+                                              ((2, 37, 3, 66), 1, 65, "BS1D"),   # odd start, 32 pairs
+                                              ((4, 50, 2, 128), 32, 96, "BS1D")])  # mid-row slice
 def test_pinned_host_buffers(dtype, shape, st, en, form):
     x, r1, r2, g = synth.case(shape, st, en, dtype, form, seed=41)
     for direction, inp in (("fwd", x), ("bwd", g)):
