@@ -1,0 +1,69 @@
+"""The fuzz draws on the CPU: every draw is a valid call, and the table draws
+reach every kernel path and access width, so the GPU fuzz test exercises
+them all.  Plans are queried with an explicit SM count on host tensors laid
+out as the GPU test lays them out (only shapes, strides and pointer
+alignment are read)."""
+import collections
+
+import pytest
+import torch
+
+import fuzz_cases as fc
+from place_partial_rope_gb300 import binding, build, synth
+from test_fuzz_gpu import GUARD, N_POS, N_QK, N_TABLE
+
+SM_COUNT = 152
+
+
+@pytest.fixture(scope="module", autouse=True)
+def lib():
+    build.build()
+    return binding.load_library()
+
+
+def host_plan(c: fc.TableCase):
+    td = synth.TORCH_DTYPE[c.dtype]
+    n = int(torch.Size(c.shape).numel())
+    x = torch.empty(c.x_offset + n + GUARD, dtype=td)[c.x_offset:c.x_offset + n].view(c.shape)
+    rs = synth.r_shape_for(c.form, c.shape, c.sl.L)
+    padded = torch.empty(rs[:3] + (c.sl.L + c.r_pad,), dtype=td)
+    r = padded[..., c.r_offset:c.r_offset + c.sl.L]
+    return binding.rope_partial_plan(x, r, r, c.sl.start, c.sl.end, SM_COUNT, c.mode)
+
+
+def test_table_draws_reach_every_path():
+    paths = collections.Counter()
+    widths = collections.Counter()
+    for k in range(N_TABLE):
+        c = fc.table_case(k)
+        plan = host_plan(c)
+        paths[plan.path] += 1
+        if plan.path:
+            widths[plan.vec_bytes] += 1
+    # 0 = nothing to do, 1 = vector accesses, 2 = element pairs,
+    # 3 = half-split lanes, 4 = 16-bit odd start with a lane per word
+    assert set(paths) == {0, 1, 2, 3, 4}, paths
+    assert {4, 8, 16} <= set(widths), widths
+    assert min(paths[p] for p in (1, 2, 3, 4)) >= 8, paths
+
+
+def test_draws_are_valid_and_varied():
+    modes, dtypes, odd = collections.Counter(), collections.Counter(), 0
+    for k in range(N_TABLE):
+        c = fc.table_case(k)
+        D, st, en = c.sl.D, c.sl.start, c.sl.end
+        assert c.shape[3] == D and 0 <= st <= en <= D and (en - st) % 2 == 0 and D % 2 == 0
+        assert 0 <= c.r_offset <= c.r_pad and int(torch.Size(c.shape).numel()) <= fc.MAX_ELEMS
+        modes[c.mode] += 1
+        dtypes[c.dtype] += 1
+        odd += st % 2
+    assert set(modes) == {"interleave", "half"} and set(dtypes) == set(synth.DTYPES)
+    assert odd >= N_TABLE // 5
+    for k in range(N_QK):
+        c = fc.qk_case(k)
+        (_, Dq, qs, qe), (_, Dk, ks, ke) = c.q, c.k
+        assert qe - qs == ke - ks and 0 <= qs <= qe <= Dq and 0 <= ks <= ke <= Dk
+        assert synth.BROADCAST_FORMS[c.form][2] == 0
+    for k in range(N_POS):
+        c = fc.pos_case(k)
+        assert c.pos_shape[0] in (1, c.shape[0]) and c.pos_shape[1] in (1, c.shape[1])
