@@ -257,7 +257,7 @@ static void row_gather_chain(int dir, int mode, float* v, const float* c, const 
 }
 
 /*
- * The same result written as one 2x2 rotation per pair (spec form),
+ * The same result written as one 2x2 rotation per pair (the explicit pair form),
  * lanes (m, n) = (2i, 2i+1) in interleave mode, (i, i + L/2) in half mode:
  *   fwd: y_m = x_m c_m - x_n s_m ;  y_n = x_n c_n + x_m s_n
  *   bwd: d_m = g_m c_m + g_n s_n ;  d_n = g_n c_n - g_m s_m
