@@ -749,7 +749,7 @@ def gpu_arm(args):
                                 "are still in L2 when the kernel ends)" if traffic else
                                 "no ncu summary for the current kernel sources"}
 
-    e2e = e2e_measure(w, x, r1, r2, g, device, min(K, 20), binding)
+    e2e = e2e_measure(w, x, r1, r2, g, device, min(K, 20), binding, world)
     ceiling = dense_rmw_ceiling(xd)
     out = {"metric": METRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": world,
            "steps": K, "warmup": args.warmup, "ms_per_step": round(1e3 * max_elapsed / K, 5),
@@ -800,7 +800,7 @@ def dense_rmw_ceiling(xd, n: int = 20) -> dict:
             "GB/s": round(2 * xd.numel() * xd.element_size() / t / 1e9, 1)}
 
 
-def e2e_measure(w, x, r1, r2, g, device, steps: int, binding):
+def e2e_measure(w, x, r1, r2, g, device, steps: int, binding, world: int = 1):
     """The same metric end to end, with inputs and results in host memory.
 
     Headline (zero copy): x, grad, cos and sin stay in page-locked host
@@ -809,7 +809,9 @@ def e2e_measure(w, x, r1, r2, g, device, steps: int, binding):
     Grace-Blackwell) and writes the rotated slice back into the host
     buffers.  The bytes crossing the link are counted from the tensors'
     slices.  For comparison, `copy_path` copies the whole tensors to device
-    buffers, runs both launches there, and copies x and grad back."""
+    buffers, runs both launches there, and copies x and grad back.  With
+    several ranks each moves its own copy of the workload over its own
+    link; the value is all ranks' bytes over the slowest rank's time."""
     e = synth.ELEM_BYTES[w.dtype]
     has_bwd = "bwd" in w.directions
     hx = synth.to_torch(x, w.dtype).pin_memory()
@@ -818,16 +820,21 @@ def e2e_measure(w, x, r1, r2, g, device, steps: int, binding):
     hs = synth.to_torch(r2, w.dtype).pin_memory()
     nl = 2 if has_bwd else 1
 
+    algo = nl * w.algorithmic_bytes()
+
     def timed(step):
+        """Per-step time of the slowest rank, and the job's GB/s."""
         step()
         torch.cuda.synchronize(device)
+        barrier(world)
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         a.record()
         for _ in range(steps):
             step()
         b.record()
         torch.cuda.synchronize(device)
-        return a.elapsed_time(b) / 1e3 / steps
+        t, total = reduce_timing(a.elapsed_time(b) / 1e3, algo * steps, world, device)
+        return t / steps, total / t / 1e9
 
     zc = [binding.prepare_fwd_host(hx, hc, hs, w.start, w.end)]
     if has_bwd:
@@ -837,7 +844,7 @@ def e2e_measure(w, x, r1, r2, g, device, steps: int, binding):
         for call in zc:
             call()
 
-    t_zc = timed(zero_copy_step)
+    t_zc, gbs_zc = timed(zero_copy_step)
     slice_bytes = w.slice_elems() * e
     r_bytes = (hc.numel() + hs.numel()) * e
 
@@ -862,16 +869,15 @@ def e2e_measure(w, x, r1, r2, g, device, steps: int, binding):
         if has_bwd:
             og.copy_(dg, non_blocking=True)
 
-    t_cp = timed(copy_step)
-    algo = nl * w.algorithmic_bytes()
-    return {"value": round(algo / t_zc / 1e9, 2), "unit": "GB/s",
+    t_cp, gbs_cp = timed(copy_step)
+    return {"value": round(gbs_zc, 2), "unit": "GB/s",
             "h2d_bytes_per_step": nl * slice_bytes + r_bytes,
             "d2h_bytes_per_step": nl * slice_bytes, "steps": steps,
             "ms_per_step": round(t_zc * 1e3, 3),
             "path": "zero copy: rope_partial_inplace_{fwd,bwd}_host on page-locked host tensors; "
                     "the kernel reads the slices and cos/sin over the host link and writes the "
                     "rotated slices back in place (one stream, synchronised at the end)",
-            "copy_path": {"value": round(algo / t_cp / 1e9, 2), "unit": "GB/s",
+            "copy_path": {"value": round(gbs_cp, 2), "unit": "GB/s",
                           "ms_per_step": round(t_cp * 1e3, 3),
                           "h2d_bytes_per_step": hx.nbytes * nl + hc.nbytes + hs.nbytes,
                           "d2h_bytes_per_step": hx.nbytes * nl,
