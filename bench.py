@@ -539,7 +539,40 @@ def breakdown(device, peak):
     out["fused_qk"] = qk_breakdown(device, peak, flush)
     out["half_split"] = half_breakdown(device, peak, flush, l2)
     out["positions"] = positions_breakdown(device, peak, flush, l2)
+    out["odd_start"] = odd_breakdown(device, peak, flush, l2)
     torch.cuda.empty_cache()
+    return out
+
+
+def odd_breakdown(device, peak, flush, l2):
+    """Odd slice starts on the gqa shape (fp16, one cos/sin row per
+    position), forward, per launch: [1, 65) has 32 pairs per row and runs a
+    lane per aligned word of x; [1, 63) has 31 and runs the element path."""
+    from place_partial_rope_gb300 import binding
+    g = synth.WORKLOADS["gqa"]
+    x = synth.normal(g.shape, g.dtype, g.seed)
+    xd = synth.to_torch(x, g.dtype).to(device)
+    e = synth.ELEM_BYTES[g.dtype]
+    out = {}
+    for st, en in ((1, 65), (1, 63)):
+        L = en - st
+        r1, r2 = synth.rope_table(synth.positions(g), L, g.dtype)
+        c, s = synth.to_torch(r1, g.dtype).to(device), synth.to_torch(r2, g.dtype).to(device)
+        call = binding.prepare_fwd(xd, c, s, st, en)
+        plan = binding.rope_partial_plan(xd, c, s, st, en)
+        for _ in range(3):
+            call()
+        t = time_launches(call, 50, flush)
+        nbytes = 2 * (xd.numel() // g.shape[3]) * L * e + 2 * r1.size * e
+        entry = {"path": int(plan.path), "cold_us": round(t * 1e6, 2),
+                 "cold_frac": round(nbytes / t / 1e9 / peak, 4)}
+        if nbytes > 1.5 * l2:
+            tb = time_back_to_back(call, 50)
+            entry["steady_us"] = round(tb * 1e6, 2)
+            entry["steady_frac"] = round(nbytes / tb / 1e9 / peak, 4)
+        out[f"gqa [{st},{en})"] = {"fwd": entry}
+        del c, s
+    del xd
     return out
 
 
