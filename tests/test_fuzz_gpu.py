@@ -5,7 +5,8 @@ slices included), a broadcast form for cos/sin, an element offset for x
 inside a larger buffer (so its base may be only element-aligned), and
 cos/sin as views into padded rows at an element offset (row strides that
 are not a multiple of any access width).  The table calls, in both rotary
-modes, and the fused query + key call must match the oracle bit for bit,
+modes, the zero-copy calls on page-locked host buffers, and the fused
+query + key call must match the oracle bit for bit,
 with the canaries around x unchanged; the call that computes cos/sin from
 positions must match within the bound its header states.  The draws are
 fixed by the seed (tests/fuzz_cases.py); a CPU test checks that they reach
@@ -22,7 +23,7 @@ from place_partial_rope_gb300 import binding, synth
 
 pytestmark = pytest.mark.gpu
 
-N_TABLE, N_QK, N_POS = 1200, 300, 300
+N_TABLE, N_QK, N_POS, N_HOST = 1200, 300, 300, 300
 GUARD = 64  # canary elements after x
 
 
@@ -65,6 +66,34 @@ def test_fuzz_table(k):
         ofn = oracle.fwd if direction == "fwd" else oracle.bwd
         want = ofn(inp, r1, r2, c.dtype, c.sl.start, c.sl.end, oracle.GATHER_CHAIN, c.mode)
         check_buffer(buf, host, c.x_offset, inp.size, c.shape, want, c.dtype, f"{c} {direction}")
+
+
+@pytest.mark.parametrize("k", range(N_HOST))
+def test_fuzz_host_buffers(k):
+    """The zero-copy calls on page-locked host tensors (interleave mode):
+    x at an element offset inside a pinned canary buffer, cos/sin as views
+    into padded pinned rows."""
+    c = fc.table_case(k)
+    x, g, r1p, r2p = fc.table_inputs(c)
+    lo, L = c.r_offset, c.sl.L
+    td = synth.TORCH_DTYPE[c.dtype]
+    c1 = synth.to_torch(r1p, c.dtype).pin_memory()[..., lo:lo + L]
+    s1 = synth.to_torch(r2p, c.dtype).pin_memory()[..., lo:lo + L]
+    r1, r2 = np.ascontiguousarray(r1p[..., lo:lo + L]), np.ascontiguousarray(r2p[..., lo:lo + L])
+    for direction, inp in (("fwd", x), ("bwd", g)):
+        host = canary(c.x_offset + inp.size + GUARD, c.dtype)
+        buf = synth.to_torch(host.copy(), c.dtype).pin_memory()
+        assert buf.dtype == td
+        view = buf[c.x_offset:c.x_offset + inp.size].view(inp.shape)
+        view.copy_(synth.to_torch(np.ascontiguousarray(inp), c.dtype))
+        fn = binding.rope_partial_inplace_fwd_host if direction == "fwd" else \
+            binding.rope_partial_inplace_bwd_host
+        fn(view, c1, s1, c.sl.start, c.sl.end)
+        torch.cuda.synchronize()
+        ofn = oracle.fwd if direction == "fwd" else oracle.bwd
+        want = ofn(inp, r1, r2, c.dtype, c.sl.start, c.sl.end)
+        check_buffer(buf, host, c.x_offset, inp.size, c.shape, want, c.dtype,
+                     f"{c} host {direction}")
 
 
 @pytest.mark.parametrize("k", range(N_QK))
