@@ -26,6 +26,7 @@ import argparse
 import ctypes
 import hashlib
 import json
+import math
 import os
 import platform
 import re
@@ -421,6 +422,27 @@ def oracle_per_workload(names=("small_model", "gqa", "mla_decode_q", "large_unal
 # the GPU arm
 # --------------------------------------------------------------------------
 
+def dram_floor_bytes(w) -> int:
+    """The fewest DRAM bytes one launch can move for this layout: every
+    row's slice read in whole 64-byte DRAM atoms and written in whole
+    32-byte sectors (the granularities the ncu counters show on this GPU:
+    352.3 MB read for the large fp32 shape's 256-byte slices at byte 136),
+    plus the unique cos and sin bytes.  Rows start at multiples of the row
+    pitch from a 256-byte aligned base."""
+    e = synth.ELEM_BYTES[w.dtype]
+    B, S, N, D = w.shape
+    rows, pitch, off, length = B * S * N, D * e, w.start * e, w.L * e
+
+    def touched(lo: int, hi: int, g: int) -> int:
+        return 0 if hi <= lo else ((hi + g - 1) // g - lo // g) * g
+
+    period = 256 // math.gcd(pitch, 256)
+    per = [touched(r * pitch + off, r * pitch + off + length, 64) +
+           touched(r * pitch + off, r * pitch + off + length, 32) for r in range(period)]
+    body = sum(per) * (rows // period) + sum(per[:rows % period])
+    return body + 2 * int(np.prod(w.r_shape)) * e
+
+
 def workload_config(w, l2_bytes: int = 132 * 2**20) -> dict:
     step = ("forward on x then backward on grad (2 launches)" if "bwd" in w.directions
             else "forward on x (1 launch)")
@@ -766,6 +788,7 @@ def gpu_arm(args):
     avg = elapsed / (nl * K)
     achieved = per_launch / avg / 1e9
     traffic = stored_traffic(kname, w.name)
+    floor = dram_floor_bytes(w)
     roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                 "frac": round(achieved / peak, 4), "traffic": traffic,
                 "peak_source": f"{peak_kind} (HBM copy bandwidth, MEASURED_PEAKS.json hbm_gbs)"
@@ -777,6 +800,12 @@ def gpu_arm(args):
                 "isolated_avg_us": {d: round(isolated[j] * 1e6, 2)
                                     for j, d in enumerate(w.directions)},
                 "algorithmic_bytes_per_launch": per_launch,
+                "dram_floor_bytes_per_launch": floor,
+                "floor_frac": round(per_launch / floor, 4),
+                "frac_of_floor": round(achieved / peak * floor / per_launch, 4),
+                "floor_note": "the fewest DRAM bytes the layout allows (64-byte read atoms, "
+                              "32-byte write sectors per row's slice, plus cos/sin); floor_frac "
+                              "is the highest frac reachable at the measured copy rate",
                 "traffic_note": "dram bytes read + written per launch, from the committed ncu "
                                 "summary of the same kernel sources (cold L2; part of the writes "
                                 "are still in L2 when the kernel ends)" if traffic else

@@ -75,3 +75,31 @@ def test_workload_config_names_the_l2_regime(name):
     big = w.algorithmic_bytes() > 1.5 * 132 * 2**20
     assert c["l2"].startswith("inputs larger than L2") == big
     assert c["l2"].startswith("NOT larger than L2") == (not big)
+
+
+def test_dram_floor_of_the_named_workloads():
+    """Aligned 128-byte slices need exactly their own bytes; the large fp32
+    shape's 256-byte slice at byte 136 of 512-byte rows touches five 64-byte
+    atoms (320 B) on the read and nine 32-byte sectors (288 B) on the write."""
+    from place_partial_rope_gb300 import synth
+    for name in ("tiny", "small_model", "gqa", "mla_decode_q"):
+        w = synth.WORKLOADS[name]
+        assert bench.dram_floor_bytes(w) == w.algorithmic_bytes(), name
+    w = synth.WORKLOADS["large_unaligned"]
+    rows = 4 * 8192 * 32
+    assert bench.dram_floor_bytes(w) == rows * (320 + 288) + 2 * 4 * 8192 * 64 * 4
+
+
+def test_dram_floor_with_rows_not_a_multiple_of_the_atom():
+    """132-byte rows (fp16, D = 66) with the slice [1, 65): the row offsets
+    cycle through every 4-byte phase of the 64-byte atom."""
+    from place_partial_rope_gb300 import synth
+    w = synth.Workload("t", "fp16", (1, 3, 5, 66), 1, 65, (1, 3, 1, 64), "arange", 0, 0, ("fwd",), "")
+    pitch, off, length = 132, 2, 128
+
+    def touched(lo, hi, g):
+        return len({b // g for b in range(lo, hi)}) * g
+
+    want = sum(touched(r * pitch + off, r * pitch + off + length, 64) +
+               touched(r * pitch + off, r * pitch + off + length, 32) for r in range(15))
+    assert bench.dram_floor_bytes(w) == want + 2 * 3 * 64 * 2
