@@ -947,6 +947,28 @@ def e2e_measure(w, x, r1, r2, g, device, steps: int, binding, world: int = 1):
                                   "buffers, x and grad copied back (one stream)"}}
 
 
+SECTIONS = {
+    "fused_qk": lambda dev, peak, flush, l2: qk_breakdown(dev, peak, flush),
+    "half_split": half_breakdown,
+    "positions": positions_breakdown,
+    "odd_start": odd_breakdown,
+}
+
+
+def run_section(name: str) -> int:
+    """One part of the breakdown on cuda:0, alone, so that a profiler sees
+    only its launches."""
+    from place_partial_rope_gb300 import build
+    build.build()
+    device = torch.device("cuda", 0)
+    torch.cuda.set_device(device)
+    peak, _ = hbm_peak()
+    l2 = torch.cuda.get_device_properties(device).L2_cache_size
+    out = SECTIONS[name](device, peak, l2_flusher(device), l2)
+    print(json.dumps({"section": name, "result": out}), flush=True)
+    return 0
+
+
 def reference_arm(args):
     world, rank, _ = dist_env()
     if rank != 0:
@@ -977,7 +999,12 @@ def main():
     ap.add_argument("--impl", choices=["native", "reference"], default="native")
     ap.add_argument("--workload", choices=sorted(synth.WORKLOADS), default=HEADLINE,
                     help="named configuration a step runs (default: the largest)")
+    ap.add_argument("--section", choices=sorted(SECTIONS),
+                    help="run only this part of the per-workload breakdown and print its JSON "
+                         "(for profiling one kernel kind; not a bench line)")
     args = ap.parse_args()
+    if args.section:
+        return run_section(args.section)
     if args.warmup < 3 and args.impl == "native":
         args.warmup = 3
     world = dist_env()[0]
