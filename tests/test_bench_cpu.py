@@ -103,3 +103,28 @@ def test_dram_floor_with_rows_not_a_multiple_of_the_atom():
     want = sum(touched(r * pitch + off, r * pitch + off + length, 64) +
                touched(r * pitch + off, r * pitch + off + length, 32) for r in range(15))
     assert bench.dram_floor_bytes(w) == want + 2 * 3 * 64 * 2
+
+
+def test_reference_arm_under_torchrun_prints_one_line_from_rank_0():
+    """`bench.py --impl reference` launched as two ranks (CPU only): rank 0
+    times the oracle and prints the one JSON line, the other rank exits 0
+    without work."""
+    import json
+    import socket
+    import subprocess
+    import sys
+
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        port = s.getsockname()[1]
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1", "--nproc-per-node", "2",
+           "--master-addr", "127.0.0.1", "--master-port", str(port), "bench.py", "--impl",
+           "reference", "--gpus", "2", "--workload", "tiny", "--steps", "2", "--warmup", "1"]
+    r = subprocess.run(cmd, cwd=root, capture_output=True, text=True, timeout=240)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [l for l in r.stdout.splitlines() if l.startswith("{")]
+    assert len(lines) == 1, r.stdout
+    out = json.loads(lines[0])
+    assert out["impl"] == "reference" and out["n_gpus"] == 2 and out["value"] > 0
+    assert out["cpu_baseline"]["kind"] == "oracle" and out["e2e"]["h2d_bytes_per_step"] == 0
