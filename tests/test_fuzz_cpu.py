@@ -67,3 +67,43 @@ def test_draws_are_valid_and_varied():
     for k in range(N_POS):
         c = fc.pos_case(k)
         assert c.pos_shape[0] in (1, c.shape[0]) and c.pos_shape[1] in (1, c.shape[1])
+
+
+def test_plans_of_the_draws_keep_their_contract():
+    """For every table draw: the work items cover each row's slice exactly
+    once, a wide access is aligned for x, cos and sin, the heads per thread
+    leave at most a quarter of head slots idle, and each path appears only
+    where it applies (rules of rope_partial_plan in include/rope_partial.h)."""
+    for k in range(N_TABLE):
+        c = fc.table_case(k)
+        plan = host_plan(c)
+        B, S, N, D = c.shape
+        e = synth.ELEM_BYTES[c.dtype]
+        L, st = c.sl.L, c.sl.start
+        what = f"{c} -> path {plan.path} vec {plan.vec_bytes} U {plan.heads_per_thread} C {plan.chunks_per_row}"
+        if plan.path == 0:
+            assert L == 0 or B * S * N == 0, what
+            continue
+        U, C, vec = plan.heads_per_thread, plan.chunks_per_row, plan.vec_bytes
+        assert U in (1, 2, 4, 8) and U <= max(N, 1), what
+        slots = -(-N // U) * U
+        assert U == 1 or (slots - N) * 4 <= slots, what
+        assert plan.tasks == B * S * (-(-N // U)) * C, what
+        half = c.mode == "half"
+        if plan.path in (1, 3):
+            # a wide access: whole chunks of the slice (of each half in half-split mode
+            # with both halves in one thread), aligned everywhere
+            covered = C * vec if (plan.path == 3 or not half) else 2 * C * vec
+            assert covered == L * e, what
+            assert (st * e) % vec == 0 and (D * e) % vec == 0, what
+            assert (c.x_offset * e) % vec == 0 and (c.r_offset * e) % vec == 0, what
+            if any(synth.BROADCAST_FORMS[c.form]):  # cos/sin rows at a stride of L + pad
+                assert ((L + c.r_pad) * e) % vec == 0, what
+            assert plan.path != 3 or half, what
+        elif plan.path == 2:
+            assert C == L // 2 and vec == (e if half else 2 * e), what
+        else:
+            assert plan.path == 4, what
+            pairs = L // 2
+            assert c.dtype != "fp32" and not half and st % 2 == 1, what
+            assert C == pairs and pairs & (pairs - 1) == 0 and pairs <= 32 and vec == 4, what
