@@ -97,7 +97,8 @@ def test_plans_of_the_draws_keep_their_contract():
             assert covered == L * e, what
             assert (st * e) % vec == 0 and (D * e) % vec == 0, what
             assert (c.x_offset * e) % vec == 0 and (c.r_offset * e) % vec == 0, what
-            if any(synth.BROADCAST_FORMS[c.form]):  # cos/sin rows at a stride of L + pad
+            rs = synth.r_shape_for(c.form, c.shape, L)
+            if rs[0] * rs[1] * rs[2] > 1:  # several cos/sin rows, at a stride of L + pad
                 assert ((L + c.r_pad) * e) % vec == 0, what
             assert plan.path != 3 or half, what
         elif plan.path == 2:
