@@ -567,34 +567,48 @@ def breakdown(device, peak):
 
 
 def odd_breakdown(device, peak, flush, l2):
-    """Odd slice starts on the gqa shape (fp16, one cos/sin row per
-    position), forward, per launch: [1, 65) has 32 pairs per row and runs a
-    lane per aligned word of x; [1, 63) has 31 and runs the element path."""
+    """Odd slice starts, forward, per launch: on the gqa shape (fp16, one
+    cos/sin row per position) [1, 65) (32 pairs per row), [1, 63) (31: the
+    row's last lane stores part of its vector) and [3, 45) (21 pairs from
+    element 3 of a vector); on the large fp32 shape (per-batch position
+    offsets) [1, 65).  A start at element 1 of a 16-byte vector runs the
+    odd-start kernel (path 4, a lane per aligned vector of x), [3, 45) the
+    element path (path 2).  Such a slice touches one more 64-byte DRAM atom
+    per row than an aligned one, so each entry also gives the layout's DRAM
+    floor and the fraction of it."""
+    import dataclasses
     from place_partial_rope_gb300 import binding
-    g = synth.WORKLOADS["gqa"]
-    x = synth.normal(g.shape, g.dtype, g.seed)
-    xd = synth.to_torch(x, g.dtype).to(device)
-    e = synth.ELEM_BYTES[g.dtype]
     out = {}
-    for st, en in ((1, 65), (1, 63)):
-        L = en - st
-        r1, r2 = synth.rope_table(synth.positions(g), L, g.dtype)
-        c, s = synth.to_torch(r1, g.dtype).to(device), synth.to_torch(r2, g.dtype).to(device)
-        call = binding.prepare_fwd(xd, c, s, st, en)
-        plan = binding.rope_partial_plan(xd, c, s, st, en)
-        for _ in range(3):
-            call()
-        t = time_launches(call, 50, flush)
-        nbytes = 2 * (xd.numel() // g.shape[3]) * L * e + 2 * r1.size * e
-        entry = {"path": int(plan.path), "cold_us": round(t * 1e6, 2),
-                 "cold_frac": round(nbytes / t / 1e9 / peak, 4)}
-        if nbytes > 1.5 * l2:
-            tb = time_back_to_back(call, 50)
-            entry["steady_us"] = round(tb * 1e6, 2)
-            entry["steady_frac"] = round(nbytes / tb / 1e9 / peak, 4)
-        out[f"gqa [{st},{en})"] = {"fwd": entry}
-        del c, s
-    del xd
+    for name, cases in (("gqa", ((1, 65), (1, 63), (3, 45))), ("large_unaligned", ((1, 65),))):
+        w0 = synth.WORKLOADS[name]
+        x = synth.normal(w0.shape, w0.dtype, w0.seed)
+        xd = synth.to_torch(x, w0.dtype).to(device)
+        pos = synth.positions(w0)
+        for st, en in cases:
+            L = en - st
+            w = dataclasses.replace(w0, start=st, end=en, r_shape=w0.r_shape[:3] + (L,))
+            r1, r2 = synth.rope_table(pos, L, w.dtype)
+            c, s = synth.to_torch(r1, w.dtype).to(device), synth.to_torch(r2, w.dtype).to(device)
+            call = binding.prepare_fwd(xd, c, s, st, en)
+            plan = binding.rope_partial_plan(xd, c, s, st, en)
+            for _ in range(3):
+                call()
+            t = time_launches(call, 50, flush)
+            nbytes = w.algorithmic_bytes()
+            floor = nbytes / dram_floor_bytes(w)
+            entry = {"path": int(plan.path), "vec_bytes": int(plan.vec_bytes),
+                     "lanes_per_row": int(plan.chunks_per_row),
+                     "heads_per_thread": int(plan.heads_per_thread),
+                     "cold_us": round(t * 1e6, 2), "cold_frac": round(nbytes / t / 1e9 / peak, 4),
+                     "floor_frac": round(floor, 4)}
+            if nbytes > 1.5 * l2:
+                tb = time_back_to_back(call, 50)
+                entry["steady_us"] = round(tb * 1e6, 2)
+                entry["steady_frac"] = round(nbytes / tb / 1e9 / peak, 4)
+                entry["steady_frac_of_floor"] = round(nbytes / tb / 1e9 / peak / floor, 4)
+            out[f"{name} [{st},{en})"] = {"fwd": entry}
+            del c, s
+        del xd
     return out
 
 

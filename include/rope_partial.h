@@ -264,6 +264,47 @@ rope_status_t rope_partial_inplace_bwd_host(void* grad, const void* r1, const vo
                                             const int64_t r2_shape[4], const int64_t r2_stride[4],
                                             int64_t start, int64_t end, rope_stream_t stream);
 
+/*
+ * Data-parallel split of the token grid (multi-GPU: one process per GPU,
+ * no collective).  Every row (b, s, n) of the operation needs only itself
+ * and its own cos/sin row, so the tokens t = b * S + s of one workload can
+ * be split across ranks with nothing exchanged: each rank rotates its own
+ * tokens' rows with its own cos/sin rows.  This follows the token-range
+ * convention of "CANN ops-transformer aclnnMoeTokenUnpermuteWithEpGrad"
+ * (lshu.cn/news/80967, section 一: under expert-parallel splitting each
+ * device handles only the tokens in [range[0], range[1])).
+ *
+ * rope_partial_token_shard gives rank `rank` of `world` the tokens
+ * [*t0, *t1) of a (B, S) grid: contiguous in b * S + s order, the first
+ * (B * S) % world ranks one token more than the others, the ranks in order
+ * tiling [0, B * S) exactly once.  It splits that range into *nruns <= 3
+ * runs, in order, each a contiguous block of a BSND tensor that one call of
+ * this library can rotate: the end of a batch entered mid-way, whole
+ * batches, the start of a batch (a range inside one batch is one run).
+ * Run k covers batches [b0, b0 + nb) x positions [s0, s0 + ns), and either
+ * nb == 1 or (s0 == 0 and ns == S).  For that call, x starts at token
+ * (b0, s0) (byte offset (b0 * S + s0) * N * D * e of the full tensor, or of
+ * the rank's own buffer of its tokens at ((b0 * S + s0) - t0) * N * D * e),
+ * the sizes are (nb, ns, N, D), and cos/sin start at their (b0, s0) row
+ * along each dim they do not broadcast, shapes (nb or 1, ns or 1, Nr, L),
+ * strides unchanged.
+ *
+ * Host only: no CUDA call.  B, S >= 0, 0 <= rank < world.  An empty grid
+ * or an empty share gives *nruns == 0 and *t0 == *t1.  Returns
+ * ROPE_ERR_NULLPTR for a null output pointer, ROPE_ERR_INVALID for
+ * negative sizes, a rank outside [0, world) or a B * S that overflows.
+ */
+typedef struct {
+    int64_t b0; /* first batch of the run                                    */
+    int64_t s0; /* first position (sequence index) in each of its batches    */
+    int64_t nb; /* batches: 1, or several whole batches                      */
+    int64_t ns; /* positions per batch of the run (S whenever nb > 1)         */
+} rope_token_run_t;
+
+rope_status_t rope_partial_token_shard(int64_t B, int64_t S, int32_t rank, int32_t world,
+                                       int64_t* t0, int64_t* t1, rope_token_run_t runs[3],
+                                       int32_t* nruns);
+
 /* A static, human-readable name of a status code. */
 const char* rope_status_str(rope_status_t status);
 

@@ -42,6 +42,12 @@ class RopePlan(ctypes.Structure):
                 ("launches", ctypes.c_int64)]
 
 
+class RopeTokenRun(ctypes.Structure):
+    """Mirror of ``rope_token_run_t``."""
+    _fields_ = [("b0", ctypes.c_int64), ("s0", ctypes.c_int64), ("nb", ctypes.c_int64),
+                ("ns", ctypes.c_int64)]
+
+
 class RopeError(RuntimeError):
     def __init__(self, status: int, message: str):
         super().__init__(message)
@@ -91,6 +97,10 @@ def load_library() -> ctypes.CDLL:
         fn.argtypes = qk
     lib.rope_partial_plan.restype = ctypes.c_int
     lib.rope_partial_plan.argtypes = args + [ctypes.c_int32, ctypes.POINTER(RopePlan)]
+    lib.rope_partial_token_shard.restype = ctypes.c_int
+    lib.rope_partial_token_shard.argtypes = [ctypes.c_int64, ctypes.c_int64, ctypes.c_int32,
+                                             ctypes.c_int32, i64p, i64p,
+                                             ctypes.POINTER(RopeTokenRun), ctypes.POINTER(ctypes.c_int32)]
     lib.rope_status_str.restype = ctypes.c_char_p
     lib.rope_status_str.argtypes = [ctypes.c_int]
     lib.rope_last_error_message.restype = ctypes.c_char_p
@@ -377,3 +387,15 @@ def rope_partial_plan(x: torch.Tensor, r1: torch.Tensor, r2: torch.Tensor, start
                                     ctypes.byref(plan))
     _raise_for(lib, st)
     return plan
+
+
+def rope_partial_token_shard(B: int, S: int, rank: int, world: int):
+    """Rank ``rank`` of ``world``'s tokens of a (B, S) grid: ``(t0, t1, runs)``
+    with runs as ``(b0, s0, nb, ns)`` tuples (host only, no CUDA call)."""
+    lib = load_library()
+    t0, t1, n = ctypes.c_int64(), ctypes.c_int64(), ctypes.c_int32()
+    runs = (RopeTokenRun * 3)()
+    st = lib.rope_partial_token_shard(B, S, rank, world, ctypes.byref(t0), ctypes.byref(t1), runs,
+                                      ctypes.byref(n))
+    _raise_for(lib, st)
+    return t0.value, t1.value, [(r.b0, r.s0, r.nb, r.ns) for r in runs[:n.value]]

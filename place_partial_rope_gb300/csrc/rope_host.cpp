@@ -146,9 +146,20 @@ rope_status_t check(const void* x, const void* r1, const void* r2, int dtype, in
 // accesses ([0, 48): 45.2 us against 49.4 at 2) and 2 otherwise, except the
 // positions call, which wants 2 (gqa 44.8 us against 47.4 at 4).  The
 // element path is best at 8 (4 with both halves in one thread).
+// The odd-start kernel (a lane per aligned vector of x, vec bytes): 4 heads
+// per thread on 16-byte vectors (the most that kernel instance allows), 8
+// on 8-byte ones.  Back to back on GB300: GQA [1, 65) 16-byte 58.0 us (U
+// = 4) against 64.0 (2); 8-byte 60.0 (8) against 68.1 (4); large fp32
+// [1, 65) 16-byte 98.8 (4) against 113.8 (2), 8-byte 106.0 (8) against
+// 127.0 (4).
+int odd_heads_cap(int e, int vec) {
+    (void)e;
+    return vec == 16 ? 4 : 8;
+}
+
 int heads_cap(int e, int vec, int path, bool pair, bool lanes, bool pos) {
     if (path == kScalarPair) return pair ? 4 : 8;
-    if (path == kOddPair) return vec;  // the caller passes the cap for this path
+    if (path == kOddPair) return odd_heads_cap(e, vec);
     if (e == 4) {
         const int per_head = pair ? 2 * vec : vec;  // bytes of x per head
         return per_head >= 32 ? 1 : 32 / per_head;
@@ -203,24 +214,53 @@ rope_status_t make_plan(int dir, int mode, int dtype, const Seg* seg, int nseg, 
     P->dir = dir;
     P->two = nseg == 2;
     P->half = half;
-    // 16-bit interleave with an odd start, rows of 1..32 pairs (a power of
-    // two): a lane per aligned word of x (the row pitch is a multiple of 4
-    // bytes since D is even; the element after the slice exists since end
-    // is odd and D even), cos/sin of pair p as their rows' aligned word p
+    // Interleave with an odd start (one tensor, table call): every pair
+    // straddles two aligned accesses.  A lane per aligned V-byte vector of x,
+    // V the widest of 16 and 8 bytes that divides x's address and its row
+    // pitch, when the slice starts at element 1 of its vector (start = 1
+    // modulo V / e; then each lane's cos/sin are the pair-aligned V bytes at
+    // its own offset): cos/sin are loaded a pair at a time (a 4-byte word per
+    // 16-bit pair, two per fp32 pair, so their rows must be 4-byte aligned),
+    // or one V-byte access per lane when their rows are V-aligned.  A lane's
+    // vector holds VE = V / e elements and the first elements of PV = VE / 2
+    // pairs, so a row takes (P - 1) / PV + 1 lanes for its P pairs.  Other
+    // odd starts run the element path, which measured faster there (back to
+    // back on GB300, GQA shape: [3, 45) 48.5 against 50.7 us; 16-bit rows only
+    // 4-byte aligned, [1, 65): 74.0 against 78.6 us; large fp32 [3, 67): 108.2
+    // against 109.6 us), while this kernel wins at [1, 65) (58.5 against
+    // 74.1 us), [1, 63) (53.9 against 58.6), the MLA-decode query's [1, 65)
+    // (32.1 against 43.0) and the large fp32 shape's [1, 65) (98.9 against
+    // 108.2).
     const int64_t pairs = R.L / 2;
-    const bool odd = !vec && !half && !pos && nseg == 1 && e == 2 && (seg[0].start & 1) &&
-                     reinterpret_cast<uintptr_t>(seg[0].x) % 4 == 0 && pairs <= 32 &&
-                     (pairs & (pairs - 1)) == 0 && p1 % 4 == 0 && p2 % 4 == 0 &&
-                     R.rb[0][0] % 4 == 0 && R.rb[0][1] % 4 == 0 && R.rb[0][2] % 4 == 0 &&
-                     R.rb[1][0] % 4 == 0 && R.rb[1][1] % 4 == 0 && R.rb[1][2] % 4 == 0;
+    int odd_v = 0;
+    if (!vec && !half && !pos && nseg == 1 && (seg[0].start & 1)) {
+        bool r4 = p1 % 4 == 0 && p2 % 4 == 0;
+        for (int r = 0; r < 2; ++r)
+            for (int k = 0; k < 3; ++k) r4 = r4 && R.rb[r][k] % 4 == 0;
+        const uintptr_t px = reinterpret_cast<uintptr_t>(seg[0].x);
+        const int64_t row = seg[0].D * e;
+        for (int v = 16; r4 && v >= 8; v /= 2)
+            if (px % v == 0 && row % v == 0) {
+                odd_v = v;
+                break;
+            }
+        // the slice must start at element 1 of its vector
+        if (odd_v && seg[0].start % (odd_v / e) != 1) odd_v = 0;
+    }
+    P->odd_wide = false;
     if (vec) {
         P->path = kVector;
         P->vec = vec;
         P->C = static_cast<int>(Lb / vec);
-    } else if (odd) {
+    } else if (odd_v) {
         P->path = kOddPair;
-        P->vec = 4;
-        P->C = static_cast<int>(pairs);
+        P->vec = odd_v;
+        const int PV = odd_v / e / 2;
+        P->C = static_cast<int>((pairs - 1) / PV + 1);
+        bool wide = p1 % odd_v == 0 && p2 % odd_v == 0;
+        for (int r = 0; r < 2; ++r)
+            for (int k = 0; k < 3; ++k) wide = wide && R.rb[r][k] % odd_v == 0;
+        P->odd_wide = wide;
     } else if (half) {
         P->path = kScalarPair;  // a 16-bit slice not aligned for 4-byte accesses
         P->vec = e;
@@ -249,12 +289,8 @@ rope_status_t make_plan(int dir, int mode, int dtype, const Seg* seg, int nseg, 
     // (1.05 ms on the full grid), mla_decode_q 0.42 against 0.45 ms; the
     // large fp32 shape 2.18 ms against 2.26-2.30 ms with 2 or 4.
     const bool pair = half && !P->lanes;
-    // the odd-start path: 8 heads per thread on rows of 16 or 32 pairs (gqa
-    // [1, 65): 69.8 us against 72.5 at 4 and 73.4 on the element path), 2 on
-    // shorter rows ([1, 17): 29.4 us against 30.1 at 4 and 33.3)
-    const int cap_vec = P->path == kOddPair ? (P->C >= 16 ? 8 : 2) : P->vec;
     P->U = choose_heads_per_thread(seg[0].N,
-                                   host ? 1 : heads_cap(e, cap_vec, P->path, pair, P->lanes, pos));
+                                   host ? 1 : heads_cap(e, P->vec, P->path, pair, P->lanes, pos));
     // Grid: for one tensor, a grid of one block per 256 work items, whose
     // blocks the hardware replaces as they finish, ran faster than a
     // resident grid whose threads stride over the work (the large fp32
@@ -287,6 +323,13 @@ KernelArgs base_args(const Plan& P, const Seg* seg, int nseg, const void* r1, co
                      const Resolved& R) {
     KernelArgs k{};
     k.x = static_cast<char*>(seg[0].x) + seg[0].start * R.e;
+    if (P.path == kOddPair) {
+        // the odd-start kernel addresses whole vectors from the one that
+        // holds element start (at its element 1)
+        k.x -= R.e;
+        k.pairs = static_cast<int32_t>(R.L / 2);
+        k.odd_wide = P.odd_wide ? 1 : 0;
+    }
     k.row_bytes = seg[0].D * R.e;
     k.tok_bytes = seg[0].N * seg[0].D * R.e;
     k.N1 = static_cast<int32_t>(seg[0].N);
@@ -616,6 +659,45 @@ rope_status_t rope_partial_inplace_bwd_host(void* grad, const void* r1, const vo
                                             int64_t end, rope_stream_t stream) {
     return rope::run(rope::kBwd, grad, r1, r2, dtype, B, S, N, D, r1_shape, r1_stride, r2_shape,
                      r2_stride, start, end, stream, true);
+}
+
+rope_status_t rope_partial_token_shard(int64_t B, int64_t S, int32_t rank, int32_t world,
+                                       int64_t* t0, int64_t* t1, rope_token_run_t runs[3],
+                                       int32_t* nruns) {
+    using namespace rope;
+    g_msg[0] = '\0';
+    if (!t0 || !t1 || !runs || !nruns) return fail(ROPE_ERR_NULLPTR, "an output pointer is null");
+    if (B < 0 || S < 0)
+        return fail(ROPE_ERR_INVALID, "negative size: B=%lld S=%lld", (long long)B, (long long)S);
+    if (world < 1 || rank < 0 || rank >= world)
+        return fail(ROPE_ERR_INVALID, "rank %d is outside [0, world=%d)", (int)rank, (int)world);
+    if (mul_overflows(B, S))
+        return fail(ROPE_ERR_INVALID, "B=%lld x S=%lld tokens overflow", (long long)B, (long long)S);
+    const int64_t T = B * S;
+    // balanced: the first T % world ranks take one token more
+    const int64_t base = T / world, rem = T % world;
+    const int64_t lo = int64_t(rank) * base + (rank < rem ? rank : rem);
+    const int64_t hi = lo + base + (rank < rem ? 1 : 0);
+    *t0 = lo;
+    *t1 = hi;
+    *nruns = 0;
+    if (lo == hi) return ROPE_OK;
+    int64_t t = lo;
+    if (t % S != 0) {  // the rest of the batch the range enters mid-way
+        const int64_t s = t % S, n = (S - s < hi - t) ? S - s : hi - t;
+        runs[(*nruns)++] = rope_token_run_t{t / S, s, 1, n};
+        t += n;
+    }
+    if (hi - t >= S) {  // whole batches
+        const int64_t nb = (hi - t) / S;
+        runs[(*nruns)++] = rope_token_run_t{t / S, 0, nb, S};
+        t += nb * S;
+    }
+    if (t < hi) {  // the start of the batch the range leaves mid-way
+        runs[(*nruns)++] = rope_token_run_t{t / S, 0, 1, hi - t};
+        t = hi;
+    }
+    return ROPE_OK;
 }
 
 const char* rope_status_str(rope_status_t status) {

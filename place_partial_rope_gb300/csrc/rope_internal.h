@@ -10,6 +10,11 @@ namespace rope {
 
 constexpr int kThreads = 256;            // threads per block
 constexpr int kBlocksPerSmCap = 8;       // 2048 resident threads per SM / 256
+// The odd-start kernel's launch bound: at least 4 resident blocks per SM
+// (64 registers a thread).  Back to back on GB300 this ran the GQA shape's
+// [1, 65) forward in 58.0 us against 64.6 us without it (68 registers, 3
+// blocks per SM) and 81 us with 5 blocks (spills).
+constexpr int kOddBlocksPerSm = 4;
 constexpr uint32_t kMaxPieceTasks = 1u << 31;  // flat work index of one launch
 constexpr int kMaxPairs = 512;           // L / 2 for the largest slice (D <= 1024)
 
@@ -30,6 +35,8 @@ enum Mode : int { kInterleave = 1, kHalf = 2 };  // the ACLNN numbering: interle
 // three fast divisions, then into byte offsets from the piece's bases.
 struct KernelArgs {
     char* x;                   // row 0 of the piece's first token, plus start * e
+                               // (odd-start kernel: plus (start - 1) * e, the
+                               // vector that holds element start)
     const char* r1;            // cos of the piece's first (batch, seq) position
     const char* r2;            // sin of the same
     int64_t tok_bytes;         // bytes between consecutive tokens of x (N * D * e)
@@ -43,7 +50,10 @@ struct KernelArgs {
     int64_t half_off;          // half-split mode: bytes from lane j to lane j + L/2
     const int32_t* pos;        // positions call: position of the piece's first (b, s)
     int64_t pos_b, pos_s;      // element strides of the positions (0: broadcast)
-    int32_t pairs;             // positions call: L / 2 entries of the FreqTable
+    int32_t pairs;             // positions call: L / 2 entries of the FreqTable;
+                               // odd-start kernel: pairs per row slice
+    int32_t odd_wide;          // odd-start kernel: cos/sin rows aligned for one
+                               // V-byte access per lane
     uint32_t tasks;            // work items of the piece: tokens * (H + H2) * C
     uint32_t tasks1;           // fused query + key call: the first tensor's items
                                // (tokens * H * C), which come before the second's
@@ -76,6 +86,8 @@ struct Plan {
     bool full_grid; // one block per 256 work items instead of a resident,
                     // grid-striding grid
     bool pos;       // cos/sin computed from positions (rope_partial_pos_kernel)
+    bool odd_wide;  // odd start (kOddPair): each lane's cos/sin is one aligned
+                    // vec-byte access
 };
 
 // The kernel instance a plan runs, or nullptr if none was compiled for it

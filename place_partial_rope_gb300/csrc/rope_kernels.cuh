@@ -510,89 +510,276 @@ __global__ void __launch_bounds__(kThreads) rope_partial_half_kernel(const Kerne
 }
 
 // ------------------------------------------------------------------------
-// 16-bit interleave mode with an odd start: pairs across aligned words
+// interleave mode with an odd start: pairs straddle aligned accesses
 // ------------------------------------------------------------------------
-// With an odd start, pair p of a row (elements start + 2p and start + 2p + 1)
-// straddles two aligned 4-byte words: the high half of word p and the low
-// half of word p + 1, counting words from the one that holds element
-// start - 1.  For rows of P pairs with P a power of two in [1, 32], lane p
-// of a row loads word p (a warp's loads are contiguous), takes the low half
-// of word p + 1 from lane p + 1 by shuffle (the row's last lane loads word P
-// itself) and stores word p whole: its low half is the previous pair's
-// second result, taken from lane p - 1 by shuffle.  The row's first lane
-// stores only the high half of word 0 and its last lane only the low half of
-// word P (2-byte stores), so no byte outside the slice is written.
-template <typename T, int U, int DIR, bool RHEAD>
-__global__ void __launch_bounds__(kThreads) rope_partial_odd_kernel(const KernelArgs a) {
-    static_assert(sizeof(T) == 2, "the odd-start path is for 16-bit storage");
+// With an odd start, the first element of every pair sits at an odd offset
+// from any aligned access of x.  This kernel takes slices that start at
+// element 1 of an aligned V-byte vector of the row (VE = V / e elements; V
+// = 16 or 8).  Lane j of a row owns the row's j-th such vector counted from
+// the one that holds element `start` (vector-relative element q = VE * j +
+// i) and rotates the PV = VE / 2 pairs whose first element lies in it:
+// pair m takes elements 2m + 1 and 2m + 2, so the last pair's second
+// element is element 0 of the next vector, brought from the next lane by
+// one shuffle.  The lane then stores its vector whole; its element 0 is the
+// previous lane's last second result, brought by one more shuffle.  Lane
+// j's pair m is slice pair w = PV * j + m (valid for w < P, the row's
+// pairs), and its cos/sin are the pair-aligned elements 2w, 2w + 1 of its
+// cos/sin row, V bytes per lane.
+//
+// Only a row's edge lanes store less: the first from element 1 (`start`)
+// on, the last up to `end`, in the fewest aligned pieces (below), so no
+// byte outside the slice is written; the last lane also stores element 0
+// of the vector after its own when the slice ends there.  A row's lanes are
+// consecutive work items, so a row may straddle two warps.  The pair that
+// straddles them belongs wholly to lane 31: it loads the next vector's
+// first word itself and stores that pair's second result there, as a row's
+// last lane does, and lane 0 of the next warp leaves its element 0 alone.
+// No lane reads an element that another lane writes, except through a
+// shuffle, so the in-place update has no race.
+//
+// Reads: whole vectors, so a row's first lane also reads element start - 1
+// and its last lane may read elements past the slice up to its vector's end,
+// and the word that holds element `end` (which exists: end is odd, D even);
+// none of them is written.
+//
+//   T   storage type    V    bytes per access of x (16 or 8)
+//   U   heads per thread     DIR  kFwd / kBwd     RHEAD  cos/sin per head
+// a.odd_wide (uniform) says the cos/sin rows are V-aligned, so a lane whose
+// pairs are all in the slice loads them with one V-byte access; otherwise
+// each pair's cos/sin is loaded by words.
+
+// Cos (or sin) of lane pairs [0, m_hi) (pair m at word m * WPP); the others
+// hold zero and nothing outside the row is read.
+template <typename T, int V>
+__device__ __forceinline__ Words<V / 4> load_lane_r(const char* row, int w0, int m_hi, bool wide) {
+    constexpr int W = V / 4;
+    constexpr int WPP = Pack<T>::kWordsPerPair;
+    constexpr int PV = W / WPP;
+    constexpr int PB = 2 * int(sizeof(T));  // bytes of one pair
+    if (wide && m_hi == PV) return ldg_vec<W>(row + int64_t(w0) * PB);
+    Words<W> r;
+#pragma unroll
+    for (int m = 0; m < PV; ++m) {
+#pragma unroll
+        for (int k = 0; k < WPP; ++k) {
+            r.w[m * WPP + k] = 0u;
+            if (m < m_hi)
+                r.w[m * WPP + k] =
+                    __ldg(reinterpret_cast<const unsigned int*>(row + int64_t(w0 + m) * PB + 4 * k));
+        }
+    }
+    return r;
+}
+
+// First and second element of lane pair m from the vector's words xw[0..W)
+// and the next vector's first word xw[W].
+template <typename T, int W>
+__device__ __forceinline__ void odd_pair_x(const uint32_t* xw, int m, float& x0, float& x1) {
+    if constexpr (sizeof(T) == 2) {
+        float lo, hi;
+        Pack<T>::get(&xw[m], lo, hi);
+        x0 = hi;  // element 2m + 1: high half of word m
+        Pack<T>::get(&xw[m + 1], lo, hi);
+        x1 = lo;  // element 2m + 2: low half of word m + 1
+    } else {
+        x0 = __uint_as_float(xw[2 * m + 1]);
+        x1 = __uint_as_float(xw[2 * m + 2]);
+    }
+}
+
+// Edge lanes of the odd-start kernel store part of their vector: elements
+// [lo, hi), lo = 0 or 1, hi odd or the whole vector.  Within one launch every
+// row's first lanes have the same range, and so do its last lanes, so a lane
+// picks its range's store sequence by value and each sequence is fixed at
+// compile time: a 2-byte store of a cut word's half at each end and the
+// whole words between in the widest aligned pieces (16, 8, 4 bytes).
+// That is the fewest stores (and L2 write requests) the range allows.  They
+// are host functions too, so that a host program can check every range.
+
+// Words [K0, K1) of sw, at p (aligned to the vector).
+template <int K0, int K1>
+__host__ __device__ __forceinline__ void store_words(char* p, const uint32_t* sw) {
+    if constexpr (K0 < K1) {
+        constexpr int n = (K0 % 4 == 0 && K1 - K0 >= 4) ? 4 : (K0 % 2 == 0 && K1 - K0 >= 2) ? 2 : 1;
+        if constexpr (n == 4)
+            *reinterpret_cast<uint4*>(p + 4 * K0) = make_uint4(sw[K0], sw[K0 + 1], sw[K0 + 2], sw[K0 + 3]);
+        else if constexpr (n == 2)
+            *reinterpret_cast<uint2*>(p + 4 * K0) = make_uint2(sw[K0], sw[K0 + 1]);
+        else
+            *reinterpret_cast<uint32_t*>(p + 4 * K0) = sw[K0];
+        store_words<K0 + n, K1>(p, sw);
+    }
+}
+
+// Elements [LO, HI) of the vector whose words are sw.
+template <typename T, int LO, int HI>
+__host__ __device__ __forceinline__ void store_span(char* p, const uint32_t* sw) {
+    if constexpr (sizeof(T) == 2) {
+        if constexpr (LO & 1)  // element LO: the high half of word LO / 2
+            *reinterpret_cast<unsigned short*>(p + 2 * LO) = static_cast<unsigned short>(sw[LO >> 1] >> 16);
+        store_words<(LO + 1) / 2, HI / 2>(p, sw);
+        if constexpr (HI & 1)  // element HI - 1: the low half of word HI / 2
+            *reinterpret_cast<unsigned short*>(p + 2 * (HI - 1)) = static_cast<unsigned short>(sw[HI >> 1] & 0xffffu);
+    } else {
+        store_words<LO, HI>(p, sw);
+    }
+}
+
+// The range by value: HI runs over VE, then the odd ends above LO.
+template <typename T, int VE, int LO, int HI>
+__host__ __device__ __forceinline__ void store_span_hi(char* p, const uint32_t* sw, int hi) {
+    if constexpr (HI <= VE) {
+        if (hi == HI) {
+            store_span<T, LO, HI>(p, sw);
+            return;
+        }
+        constexpr int first_odd = (LO & 1) ? LO + 2 : 1;
+        constexpr int next = HI == VE ? first_odd : HI + 2;
+        if constexpr (next < VE) store_span_hi<T, VE, LO, next>(p, sw, hi);
+    }
+}
+
+// LO is 0 or 1.
+template <typename T, int VE>
+__host__ __device__ __forceinline__ void store_span_lo(char* p, const uint32_t* sw, int lo, int hi) {
+    if (lo == 0) store_span_hi<T, VE, 0, VE>(p, sw, hi);
+    else store_span_hi<T, VE, 1, VE>(p, sw, hi);
+}
+
+template <typename T, int V, int U, int DIR, bool RHEAD>
+__global__ void __launch_bounds__(kThreads, kOddBlocksPerSm) rope_partial_odd_kernel(const KernelArgs a) {
     using P = Pack<T>;
-    const uint32_t C = a.divC.d;  // pairs (= lanes) per row: a power of two in [1, 32]
+    constexpr int W = V / 4;             // words per vector
+    constexpr int WPP = P::kWordsPerPair;
+    constexpr int PV = W / WPP;          // pair slots per lane
+    constexpr int VE = 2 * PV;           // elements per vector
+    static_assert(PV >= 1, "a vector holds at least one pair slot");
+    const int npairs = a.pairs;          // pairs per row slice
+    const bool wide = a.odd_wide != 0;
+    const uint32_t C = a.divC.d;         // lanes per row
     const uint32_t lane = threadIdx.x & 31u;
     const uint64_t stride = uint64_t(gridDim.x) * kThreads;
+
     enter_after_predecessor();
-    for (uint64_t t = uint64_t(blockIdx.x) * kThreads + threadIdx.x; t < a.tasks; t += stride) {
-        // the lanes of this warp still in the loop (tasks is a multiple of C,
-        // so they hold whole rows)
-        const uint64_t left = a.tasks - (t - lane);
-        const uint32_t mask = left >= 32 ? 0xffffffffu : ((1u << uint32_t(left)) - 1u);
-        uint32_t rest, p, tok, hg, b, s;
-        a.divC.divmod(uint32_t(t), rest, p);
+    // Whole warps run the loop together, so every shuffle takes all 32
+    // lanes; a lane past the end of the work ("dead") reads and writes
+    // nothing.  tasks is a multiple of C, so a live lane's next lane in the
+    // same row is live too (or in the next warp).
+    for (uint64_t base = uint64_t(blockIdx.x) * kThreads + (threadIdx.x & ~31u); base < a.tasks;
+         base += stride) {
+        const bool live = base + lane < a.tasks;
+        const uint32_t t = uint32_t(live ? base + lane : base);
+        uint32_t rest, j, tok, hg, b, s;
+        a.divC.divmod(t, rest, j);
         a.divH.divmod(rest, tok, hg);
         a.divS.divmod(tok, b, s);
-        const bool first = p == 0, last = p + 1 == C;
+
+        const int w0 = int(j) * PV;                   // slice pair of lane pair 0
+        const int m_hi = npairs - w0 < PV ? npairs - w0 : PV;  // lane pairs [0, m_hi) are in the slice
+        // element 0 is in the slice and its pair's first element is in the
+        // previous lane of this warp (which sends the result up)
+        const bool prev_here = j > 0 && lane != 0u;
+        const bool ends_next = m_hi == PV;            // pair PV-1 ends in the next vector
+        // ... and this lane stores that element: no next lane in the row, or
+        // the next lane is in another warp
+        const bool store_next = ends_next && (j + 1 == C || lane == 31u);
+        // the elements of its vector the lane stores: all of them, or (a row's
+        // edge lanes) [lo_e, hi_e)
+        const int lo_e = prev_here ? 0 : 1;
+        const int hi_e = 2 * m_hi + 1 < VE ? 2 * m_hi + 1 : VE;
+        const bool full = lo_e == 0 && hi_e == VE;
         const int n0 = int(hg) * U;
-        // word p of head n0's row: row elements start - 1 + 2p (low half)
-        // and start + 2p (high half)
-        char* w0 = a.x - 2 + int64_t(tok) * a.tok_bytes + int64_t(n0) * a.row_bytes + int64_t(p) * 4;
-        const char* c_p = a.r1 + int64_t(b) * a.r1_b + int64_t(s) * a.r1_s + int64_t(p) * 4;
-        const char* s_p = a.r2 + int64_t(b) * a.r2_b + int64_t(s) * a.r2_s + int64_t(p) * 4;
+        char* v0p = a.x + int64_t(tok) * a.tok_bytes + int64_t(n0) * a.row_bytes + int64_t(j) * V;
+        const char* c_row = a.r1 + int64_t(b) * a.r1_b + int64_t(s) * a.r1_s;
+        const char* s_row = a.r2 + int64_t(b) * a.r2_b + int64_t(s) * a.r2_s;
         if constexpr (RHEAD) {
-            c_p += int64_t(n0) * a.r1_n;
-            s_p += int64_t(n0) * a.r2_n;
+            c_row += int64_t(n0) * a.r1_n;
+            s_row += int64_t(n0) * a.r2_n;
         }
 
-        uint32_t xw[U], xn[U];  // word p, and word p + 1 for the row's last lane
+        // loads (dead lanes and heads past N read nothing and hold zeros)
+        Words<W> xv[U];
+        uint32_t xn[U];  // the next vector's first word, where this lane stores into it
 #pragma unroll
         for (int i = 0; i < U; ++i) {
-            xw[i] = 0u;
+            xv[i] = Words<W>{};
             xn[i] = 0u;
-            if (i == 0 || n0 + i < a.N) {
-                xw[i] = ld_vec<1>(w0 + i * a.row_bytes).w[0];
-                if (last) xn[i] = ld_vec<1>(w0 + i * a.row_bytes + 4).w[0];
+            if (live && (i == 0 || n0 + i < a.N)) {
+                char* p = v0p + int64_t(i) * a.row_bytes;
+                xv[i] = ld_vec<W>(p);
+                if (store_next) xn[i] = ld_vec<1>(p + V).w[0];
             }
         }
-        uint32_t cw = 0u, sw = 0u;
+        Words<W> cv{}, sv{};
         if constexpr (!RHEAD) {
-            cw = ldg_vec<1>(c_p).w[0];
-            sw = ldg_vec<1>(s_p).w[0];
+            if (live) {
+                cv = load_lane_r<T, V>(c_row, w0, m_hi, wide);
+                sv = load_lane_r<T, V>(s_row, w0, m_hi, wide);
+            }
         }
+
 #pragma unroll
         for (int i = 0; i < U; ++i) {
-            // every lane of `mask` shuffles, outside any per-lane condition
-            const uint32_t down = __shfl_down_sync(mask, xw[i], 1);
-            const uint32_t nxt = last ? xn[i] : down;
+            const bool head = live && (i == 0 || n0 + i < a.N);
+            const uint32_t down = __shfl_down_sync(0xffffffffu, xv[i].w[0], 1);
+            uint32_t xw[W + 1];
+#pragma unroll
+            for (int k = 0; k < W; ++k) xw[k] = xv[i].w[k];
+            xw[W] = store_next ? xn[i] : down;
             if constexpr (RHEAD) {
-                if (i == 0 || n0 + i < a.N) {
-                    cw = ldg_vec<1>(c_p + int64_t(i) * a.r1_n).w[0];
-                    sw = ldg_vec<1>(s_p + int64_t(i) * a.r2_n).w[0];
+                if (head) {
+                    cv = load_lane_r<T, V>(c_row + int64_t(i) * a.r1_n, w0, m_hi, wide);
+                    sv = load_lane_r<T, V>(s_row + int64_t(i) * a.r2_n, w0, m_hi, wide);
                 }
             }
-            float lo, x0, x1, hi, c0, c1, s0, s1, y0, y1;
-            P::get(&xw[i], lo, x0);  // x0: element start + 2p
-            P::get(&nxt, x1, hi);    // x1: element start + 2p + 1
-            P::get(&cw, c0, c1);
-            P::get(&sw, s0, s1);
-            rotate_pair<DIR>(x0, x1, c0, c1, s0, s1, y0, y1);
-            const uint32_t y0b = Elem<T>::put(y0), y1b = Elem<T>::put(y1);
-            const uint32_t prev = __shfl_up_sync(mask, y1b, 1);  // the previous pair's second result
-            if (i == 0 || n0 + i < a.N) {
-                char* wp = w0 + i * a.row_bytes;
-                if (first) {
-                    st_elem_scalar<T>(wp + 2, Words<1>{{y0b}});
-                } else {
-                    st_vec<1>(wp, Words<1>{{(prev & 0xffffu) | (y0b << 16)}});
+
+            // the lane's pairs: f0[m], f1[m] are pair m's first and second
+            // results in fp32
+            float f0[PV], f1[PV];
+#pragma unroll
+            for (int m = 0; m < PV; ++m) {
+                float x0, x1, c0, c1, s0, s1;
+                odd_pair_x<T, W>(xw, m, x0, x1);
+                P::get(&cv.w[m * WPP], c0, c1);
+                P::get(&sv.w[m * WPP], s0, s1);
+                rotate_pair<DIR>(x0, x1, c0, c1, s0, s1, f0[m], f1[m]);
+            }
+            // element 0: the previous lane's last second result
+            const float prev = __uint_as_float(__shfl_up_sync(0xffffffffu, __float_as_uint(f1[PV - 1]), 1));
+
+            // the vector as stored: word k holds elements 2k and 2k + 1, the
+            // second result of pair k - 1 and the first of pair k (16-bit),
+            // or element k (fp32)
+            uint32_t sw[W];
+            if constexpr (sizeof(T) == 2) {
+                P::put(&sw[0], prev, f0[0]);
+#pragma unroll
+                for (int k = 1; k < W; ++k) P::put(&sw[k], f1[k - 1], f0[k]);
+            } else {
+                sw[0] = __float_as_uint(prev);
+#pragma unroll
+                for (int m = 0; m < PV; ++m) {
+                    sw[2 * m + 1] = __float_as_uint(f0[m]);
+                    if (2 * m + 2 < W) sw[2 * m + 2] = __float_as_uint(f1[m]);
                 }
-                if (last) st_elem_scalar<T>(wp + 4, Words<1>{{y1b}});
+            }
+            if (head) {
+                char* p = v0p + int64_t(i) * a.row_bytes;
+                if (full) {
+                    Words<W> o;
+#pragma unroll
+                    for (int k = 0; k < W; ++k) o.w[k] = sw[k];
+                    st_vec<W>(p, o);
+                } else {
+                    store_span_lo<T, VE>(p, sw, lo_e, hi_e);
+                }
+                // the last pair's second result opens the next vector
+                if (store_next) {
+                    if constexpr (sizeof(T) == 2)
+                        *reinterpret_cast<unsigned short*>(p + V) = static_cast<unsigned short>(Elem<T>::put(f1[PV - 1]));
+                    else
+                        *reinterpret_cast<uint32_t*>(p + V) = __float_as_uint(f1[PV - 1]);
+                }
             }
         }
     }
@@ -889,15 +1076,11 @@ const void* pick_dir(const Plan& p) {
         return f ? reinterpret_cast<const void*>(&rope_partial_pos_kernel<T, VEC, SCALAR, U, kFwd, H>)
                  : reinterpret_cast<const void*>(&rope_partial_pos_kernel<T, VEC, SCALAR, U, kBwd, H>);
     } else if constexpr (K == kOdd) {
-        if constexpr (sizeof(T) == 2) {
-            if (f)
-                return p.r_head ? reinterpret_cast<const void*>(&rope_partial_odd_kernel<T, U, kFwd, true>)
-                                : reinterpret_cast<const void*>(&rope_partial_odd_kernel<T, U, kFwd, false>);
-            return p.r_head ? reinterpret_cast<const void*>(&rope_partial_odd_kernel<T, U, kBwd, true>)
-                            : reinterpret_cast<const void*>(&rope_partial_odd_kernel<T, U, kBwd, false>);
-        } else {
-            return nullptr;
-        }
+        if (f)
+            return p.r_head ? reinterpret_cast<const void*>(&rope_partial_odd_kernel<T, VEC, U, kFwd, true>)
+                            : reinterpret_cast<const void*>(&rope_partial_odd_kernel<T, VEC, U, kFwd, false>);
+        return p.r_head ? reinterpret_cast<const void*>(&rope_partial_odd_kernel<T, VEC, U, kBwd, true>)
+                        : reinterpret_cast<const void*>(&rope_partial_odd_kernel<T, VEC, U, kBwd, false>);
     } else if constexpr (K == kQK) {
         return f ? reinterpret_cast<const void*>(&rope_partial_qk_kernel<T, VEC, SCALAR, U, kFwd>)
                  : reinterpret_cast<const void*>(&rope_partial_qk_kernel<T, VEC, SCALAR, U, kBwd>);
@@ -980,8 +1163,11 @@ const void* pick_half(const Plan& p) {
 template <typename T>
 const void* pick_kernel(const Plan& p) {
     if (p.path == kOddPair) {
-        if constexpr (sizeof(T) == 2) return pick_heads<T, 4, false, kOdd>(p);
-        else return nullptr;
+        switch (p.vec) {
+            case 16: return pick_heads<T, 16, false, kOdd>(p);
+            case 8: return pick_heads<T, 8, false, kOdd>(p);
+            default: return nullptr;
+        }
     }
     if (p.pos) return p.half ? pick_half<T, kPosHalf>(p) : pick_interleave<T, kPos>(p);
     if (p.half) return p.lanes ? pick_half_lanes<T>(p) : pick_half<T, kHalfSplit>(p);

@@ -120,10 +120,14 @@ def table_case(k: int) -> TableCase:
     sl = _slice(rng, D, aligned=aligned)
     odd_words = not aligned and rng.random() < 0.25
     if odd_words:
-        # an odd start on a row of 1..32 pairs (a power of two), with x and
-        # the cos/sin rows 4-byte aligned
+        # an odd start with x and the cos/sin rows aligned to 4 bytes or more
+        # (the odd-start kernel's lane per aligned vector of x): half the
+        # slices a power-of-two number of pairs up to 32, half any length
         D = int(rng.choice([d for d in HEAD_DIMS if d >= 4]))
-        L = 2 * int(2 ** rng.integers(0, min(5, int(np.log2((D - 2) // 2))) + 1))
+        if rng.random() < 0.5:
+            L = 2 * int(2 ** rng.integers(0, min(5, int(np.log2((D - 2) // 2))) + 1))
+        else:
+            L = 2 * int(rng.integers(1, (D - 2) // 2 + 1))
         start = 2 * int(rng.integers(0, (D - L) // 2)) + 1
         sl = Slice(D, start, start + L)
     B, S, N = _bsn(rng, D)
@@ -131,7 +135,7 @@ def table_case(k: int) -> TableCase:
     if aligned:
         x_offset, r_offset, r_pad = 0, 0, int(rng.choice([0, 0, 8, 16]))
     elif odd_words:
-        x_offset, r_offset = 2 * int(rng.integers(0, 3)), 2 * int(rng.integers(0, 2))
+        x_offset, r_offset = 2 * int(rng.integers(0, 5)), 2 * int(rng.integers(0, 2))
         r_pad = r_offset + 2 * int(rng.integers(0, 3))
     else:
         x_offset, r_offset = int(rng.integers(0, 5)), int(rng.integers(0, 4))

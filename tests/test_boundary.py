@@ -65,7 +65,7 @@ def test_header_symbols_are_exported(lib):
                      "rope_partial_inplace_fwd_qk", "rope_partial_inplace_bwd_qk",
                      "rope_partial_inplace_fwd_mode", "rope_partial_inplace_bwd_mode",
                      "rope_partial_inplace_fwd_pos", "rope_partial_inplace_bwd_pos",
-                     "rope_partial_plan_mode",
+                     "rope_partial_plan_mode", "rope_partial_token_shard",
                      "rope_status_str", "rope_last_error_message", "rope_partial_plan"}
     for n in names:
         assert hasattr(lib, n), n
@@ -174,16 +174,33 @@ def test_plans_of_the_named_workloads(lib):
 
 def test_path_choice(lib):
     ODD = 4
-    # 16-bit odd start, rows of 1..32 pairs (a power of two): a lane per aligned word
-    p = plan(lib, start=1, end=9)
-    assert (p.path, p.vec_bytes, p.chunks_per_row, p.heads_per_thread) == (ODD, 4, 4, 2)
+    # odd start at element 1 of an aligned 16- or 8-byte vector of x (the
+    # widest that divides x's address and its row pitch): a lane per vector
+    p = plan(lib, start=1, end=9)                                     # 4 pairs in one lane
+    assert (p.path, p.vec_bytes, p.chunks_per_row, p.heads_per_thread) == (ODD, 16, 1, 2)
     p = plan(lib, dtype=FP16, shape=(32, 2048, 16, 128), start=1, end=65, r_shape=(1, 2048, 1, 64))
-    assert (p.path, p.chunks_per_row, p.heads_per_thread) == (ODD, 32, 8)
+    assert (p.path, p.vec_bytes, p.chunks_per_row, p.heads_per_thread) == (ODD, 16, 8, 4)
     assert p.blocks == p.tasks // 256
-    assert plan(lib, shape=(2, 4, 3, 16), start=1, end=7, r_shape=(1, 4, 1, 6)).path == 2  # 3 pairs
+    p = plan(lib, dtype=FP16, shape=(32, 2048, 16, 128), start=1, end=63, r_shape=(1, 2048, 1, 62))
+    assert (p.path, p.vec_bytes, p.chunks_per_row) == (ODD, 16, 8)   # 31 pairs: last lane partial
+    p = plan(lib, dtype=FP16, shape=(2, 4, 3, 64), start=9, end=51, r_shape=(1, 4, 1, 42))
+    assert (p.path, p.vec_bytes, p.chunks_per_row) == (ODD, 16, 6)    # 21 pairs
+    p = plan(lib, shape=(2, 4, 3, 16), start=1, end=7, r_shape=(1, 4, 1, 6))
+    assert (p.path, p.vec_bytes, p.chunks_per_row) == (ODD, 16, 1)    # 3 pairs
+    p = plan(lib, start=1, end=9, x=BASE + 8)                         # x only 8-byte aligned
+    assert (p.path, p.vec_bytes, p.chunks_per_row, p.heads_per_thread) == (ODD, 8, 2, 2)
+    p = plan(lib, dtype=FP32, start=1, end=9)                         # fp32: 2 pairs per lane
+    assert (p.path, p.vec_bytes, p.chunks_per_row) == (ODD, 16, 2)
+    p = plan(lib, dtype=FP32, start=1, end=9, x=BASE + 8)             # fp32: 1 pair per lane
+    assert (p.path, p.vec_bytes, p.chunks_per_row) == (ODD, 8, 4)
+    # other odd starts take the element path
+    assert plan(lib, start=3, end=11).path == 2                      # element 3 of its vector
+    assert plan(lib, start=1, end=9, x=BASE + 4).path == 2           # x only 4-byte aligned
+    assert plan(lib, shape=(2, 4, 3, 18), start=1, end=9).path == 2  # 36-byte rows
     assert plan(lib, start=1, end=9, x=BASE + 2).path == 2           # x only 2-byte aligned
     assert plan(lib, start=1, end=9, r1=BASE + 2**30 + 2).path == 2  # cos only 2-byte aligned
-    assert plan(lib, dtype=FP32, start=1, end=9).path == 2          # fp32 odd start: scalar pairs
+    assert plan(lib, dtype=FP32, start=3, end=11).path == 2          # fp32, element 3
+    assert plan(lib, dtype=FP32, start=1, end=9, x=BASE + 4).path == 2   # fp32 needs 8 bytes
     assert plan(lib, start=2, end=10).vec_bytes == 4                 # 4-byte slice offset
     assert plan(lib, x=BASE + 8).vec_bytes == 8                      # x only 8-byte aligned
     assert plan(lib, r1=BASE + 2**30 + 4).vec_bytes == 4             # cos only 4-byte aligned
@@ -209,7 +226,7 @@ def test_heads_per_thread(lib, N, vec, U):
 @pytest.mark.parametrize("start,end,mode,vec,U", [
     (32, 96, 1, 16, 2),    # fp32 16-byte accesses: 32 bytes of x per thread
     (34, 98, 1, 8, 4),     # 8-byte accesses
-    (1, 65, 1, 8, 8),      # odd start: the element path
+    (1, 65, 1, 16, 4),     # odd start: a lane per aligned 16-byte vector (4 heads)
     (34, 98, 2, 8, 4),     # half-split, partner in another lane (32 accesses per row)
     (0, 96, 2, 16, 1),     # half-split, 48 lanes per half = 12 accesses: both halves in one thread
     (2, 98, 2, 8, 2),      # 24 accesses per half of 8 bytes: both halves in one thread

@@ -41,10 +41,25 @@ def test_table_draws_reach_every_path():
         if plan.path:
             widths[plan.vec_bytes] += 1
     # 0 = nothing to do, 1 = vector accesses, 2 = element pairs,
-    # 3 = half-split lanes, 4 = 16-bit odd start with a lane per word
+    # 3 = half-split lanes, 4 = odd start with a lane per aligned vector
     assert set(paths) == {0, 1, 2, 3, 4}, paths
     assert {4, 8, 16} <= set(widths), widths
     assert min(paths[p] for p in (1, 2, 3, 4)) >= 8, paths
+
+
+def test_odd_start_draws_reach_every_vector_width():
+    """The odd-start kernel is drawn for every storage type and vector
+    width, on rows that straddle warps and rows that do not."""
+    seen, straddle = collections.Counter(), 0
+    for k in range(N_TABLE):
+        c = fc.table_case(k)
+        plan = host_plan(c)
+        if plan.path != 4:
+            continue
+        seen[(synth.ELEM_BYTES[c.dtype], plan.vec_bytes)] += 1
+        straddle += 32 % plan.chunks_per_row != 0
+    assert set(seen) == {(2, 16), (2, 8), (4, 16), (4, 8)}, seen
+    assert straddle >= 8, straddle
 
 
 def test_draws_are_valid_and_varied():
@@ -104,7 +119,14 @@ def test_plans_of_the_draws_keep_their_contract():
         elif plan.path == 2:
             assert C == L // 2 and vec == (e if half else 2 * e), what
         else:
+            # a lane per aligned vector of x: the slice starts at element 1
+            # of its vector, whose VE elements hold the first elements of
+            # VE / 2 pairs, so a row of P pairs takes (P - 1) // (VE / 2) + 1
+            # lanes
             assert plan.path == 4, what
-            pairs = L // 2
-            assert c.dtype != "fp32" and not half and st % 2 == 1, what
-            assert C == pairs and pairs & (pairs - 1) == 0 and pairs <= 32 and vec == 4, what
+            assert not half and st % 2 == 1, what
+            assert vec in (16, 8), what
+            assert (c.x_offset * e) % vec == 0 and (D * e) % vec == 0, what
+            VE = vec // e
+            assert st % VE == 1, what
+            assert C == (L // 2 - 1) // (VE // 2) + 1, what

@@ -37,7 +37,7 @@ SWEEP = [
     ((2, 5, 3, 64), 8, 40, "B11D"),
     ((2, 5, 3, 64), 2, 58, "111D"),       # 4-byte (16-bit) / 8-byte (fp32) slice offset
     ((2, 5, 3, 64), 34, 62, "BSND"),      # cos/sin per head
-    ((2, 5, 3, 64), 3, 61, "BS1D"),       # odd start: scalar pairs
+    ((2, 5, 3, 64), 3, 61, "BS1D"),       # odd start
     ((2, 5, 7, 48), 1, 3, "B1ND"),        # one pair per row, odd start
     ((1, 1, 1, 2), 0, 2, "111D"),         # D = 2
     ((3, 1, 1, 6), 4, 6, "B11D"),         # 12-byte rows
@@ -63,34 +63,73 @@ def test_sweep(dtype, k):
 
 
 ODD_STARTS = [
-    # 16-bit rows with an odd start: rows of 1..32 pairs (a power of two)
-    # run a lane per aligned word of x (path 4), the others the element
-    # path (path 2); idle head slots, the slice ending one element before
-    # the row's end, cos/sin per head, one pair per row
-    ((2, 5, 3, 64), 1, 63, "BS1D", 2),       # 31 pairs; ends at D - 1
-    ((2, 5, 3, 64), 3, 35, "B11D", 4),       # 16 pairs
-    ((2, 5, 6, 64), 5, 17, "1S1D", 2),       # 6 pairs; 6 heads
-    ((2, 4, 5, 40), 7, 39, "BSND", 4),       # 16 pairs, cos/sin per head
-    ((1, 3, 9, 8), 1, 7, "1SND", 2),         # 3 pairs, cos/sin per head
-    ((3, 2, 4, 4), 1, 3, "B1ND", 4),         # one pair per row, ends at D - 1
-    ((1, 7, 2, 1024), 1, 1023, "1S1D", 2),   # the longest odd slice
-    ((2, 3, 16, 128), 33, 97, "BS1D", 4),    # gqa-like rows, 32 pairs, U = 8
-    ((2, 3, 13, 66), 1, 65, "BS1D", 4),      # 13 heads (idle slots at U = 8)
-    ((1, 5, 6, 20), 3, 19, "BSND", 4),       # 8 pairs: 4 rows per warp
+    # shape, start, end, broadcast form, x's element offset in its buffer.
+    # An odd start at element 1 of an aligned 16- or 8-byte vector of x runs
+    # a lane per vector (path 4), any other odd start the element path (path
+    # 2); odd_path() below states the rule.  Cases: the last lane storing part
+    # of its vector, the slice ending one element before the row's end, idle
+    # head slots, cos/sin per head, one pair per row, rows whose lanes
+    # straddle two warps, and x aligned to 16, 8 or 4 bytes only.
+    ((2, 5, 3, 64), 1, 63, "BS1D", 0),       # 31 pairs; ends at D - 1
+    ((2, 5, 3, 64), 3, 35, "B11D", 0),       # 16 pairs from element 3
+    ((2, 5, 6, 64), 5, 17, "1S1D", 0),       # 6 pairs from element 5; 6 heads
+    ((2, 4, 5, 40), 7, 39, "BSND", 0),       # from element 7; cos/sin per head
+    ((1, 3, 9, 8), 1, 7, "1SND", 0),         # 3 pairs, cos/sin per head
+    ((3, 2, 4, 4), 1, 3, "B1ND", 0),         # one pair per row, ends at D - 1
+    ((1, 7, 2, 1024), 1, 1023, "1S1D", 0),   # the longest odd slice: rows span warps
+    ((2, 3, 16, 128), 33, 97, "BS1D", 0),    # gqa-like rows, 32 pairs
+    ((2, 3, 13, 66), 1, 65, "BS1D", 0),      # 13 heads (idle slots), 132-byte rows
+    ((1, 5, 6, 20), 3, 19, "BSND", 0),       # 8 pairs, cos/sin per head
+    ((3, 7, 5, 48), 1, 41, "BS1D", 0),       # 5 or 10 lanes per row: rows straddle warps
+    ((2, 3, 7, 64), 17, 59, "BS1D", 0),      # 21 pairs: 6 or 11 lanes per row
+    ((2, 9, 7, 48), 3, 45, "11ND", 0),       # cos/sin per head
+    ((2, 9, 7, 40), 3, 37, "B11D", 2),       # x 4-byte (16-bit) / 8-byte (fp32) aligned
+    ((2, 9, 7, 40), 5, 35, "1S1D", 4),       # x 8-byte / 16-byte aligned
+    ((3, 4, 5, 48), 9, 45, "B11D", 4),       # 8-byte vectors, 9 lanes per row
+    ((4, 6, 3, 96), 9, 83, "BSND", 6),       # x 4-byte / 8-byte aligned, cos/sin per head
+    ((2, 5, 3, 64), 1, 63, "BS1D", 1),       # x only element-aligned: the element path
 ]
 
 
-@pytest.mark.parametrize("dtype", ["bf16", "fp16"])
+def odd_path(shape, start, off, dtype):
+    """4 when the slice starts at element 1 of the widest 16- or 8-byte
+    vector that divides x's address (buffer base + off elements) and its row
+    pitch, else 2."""
+    e = synth.ELEM_BYTES[dtype]
+    for v in (16, 8):
+        if (off * e) % v == 0 and (shape[3] * e) % v == 0:
+            return 4 if start % (v // e) == 1 else 2
+    return 2
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "fp16", "fp32"])
 @pytest.mark.parametrize("k", range(len(ODD_STARTS)))
-def test_odd_starts_16bit(dtype, k):
-    shape, st, en, form, path = ODD_STARTS[k]
+def test_odd_starts(dtype, k):
+    """Odd starts, bit for bit against the oracle, with 4 KiB canaries on
+    both sides of x that must stay unchanged."""
+    shape, st, en, form, off = ODD_STARTS[k]
     x, r1, r2, g = synth.case(shape, st, en, dtype, form, seed=1500 + k)
-    assert binding.rope_partial_plan(to_dev(x, dtype), to_dev(r1, dtype), to_dev(r2, dtype),
-                                     st, en).path == path
+    e = synth.ELEM_BYTES[dtype]
+    guard, n = 4096 // e, x.size
+    canary = np.full(guard * 2 + off + n, 0x5A5A5A5A if e == 4 else 0x5A5A,
+                     dtype=np.uint32 if e == 4 else np.uint16)
+    canary = canary.view(np.float32) if dtype == "fp32" else canary
+    buf = to_dev(canary, dtype)
+    c, s = to_dev(r1, dtype), to_dev(r2, dtype)
+    lo = guard + off
+    view = buf[lo:lo + n].view(shape)
+    plan = binding.rope_partial_plan(view, c, s, st, en)
+    assert plan.path == odd_path(shape, st, off, dtype), (plan.path, plan.vec_bytes)
     for direction, inp in (("fwd", x), ("bwd", g)):
-        got = run_cuda(direction, inp, r1, r2, dtype, st, en)
-        want = run_oracle(direction, inp, r1, r2, dtype, st, en)
-        assert_same(got, want, dtype, f"{shape} [{st},{en}) {form} {direction}")
+        view.copy_(synth.to_torch(inp, dtype).to(DEV))
+        fn = binding.rope_partial_inplace_fwd if direction == "fwd" else binding.rope_partial_inplace_bwd
+        fn(view, c, s, st, en)
+        torch.cuda.synchronize()
+        host = synth.from_torch(buf)
+        assert_same(host[lo:lo + n].reshape(shape), run_oracle(direction, inp, r1, r2, dtype, st, en),
+                    dtype, f"{shape} [{st},{en}) {form} offset {off} {direction}")
+        assert np.array_equal(host[:lo], canary[:lo]), "canary before x changed"
+        assert np.array_equal(host[lo + n:], canary[lo + n:]), "canary after x changed"
 
 
 @pytest.mark.parametrize("dtype", ["bf16", "fp16", "fp32"])
