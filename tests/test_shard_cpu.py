@@ -168,3 +168,45 @@ def test_weak_scaling_gives_each_rank_the_named_workload_size():
             assert sh.tokens == 4 * 8192 and len(sh.runs) == 1 and sh.runs[0].nb == 4
     g = shard.weak_workload(synth.WORKLOADS["gqa"], 4)
     assert g.shape == (128, 2048, 16, 128) and g.r_shape == (1, 2048, 1, 64)
+
+
+def test_bench_rank_calls_cover_each_run_in_order():
+    """bench.py's step on one rank: every direction over every run of the
+    rank's share, forward first, each on the run's block of the rank's
+    buffer and the run's own cos/sin rows (a fake binding records them)."""
+    import torch
+
+    import bench
+
+    class Fake:
+        calls = []
+
+        @staticmethod
+        def _rec(name):
+            def prep(buf, c, s, start, end):
+                Fake.calls.append((name, tuple(buf.shape), buf.data_ptr(), tuple(c.shape), start, end))
+                return lambda: None
+            return prep
+
+    Fake.prepare_fwd, Fake.prepare_bwd = Fake._rec("fwd"), Fake._rec("bwd")
+    Fake.prepare_fwd_host, Fake.prepare_bwd_host = Fake._rec("fwd_host"), Fake._rec("bwd_host")
+    w = SMALL[3]  # (2, 7, 2, 10) [3, 9), per-batch cos/sin rows, forward and backward
+    for world in (1, 3):
+        for rank in range(world):
+            ri = shard.rank_inputs(w, rank, world, weak=False)
+            x, g = torch.from_numpy(ri.x.view(np.int16)), torch.from_numpy(ri.g.view(np.int16))
+            tabs = [(torch.from_numpy(c.view(np.int16)), torch.from_numpy(s.view(np.int16)))
+                    for c, s in ri.tables]
+            for host in (False, True):
+                Fake.calls = []
+                calls = bench.rank_calls(Fake, shard, ri, {"fwd": x, "bwd": g}, tabs, w, host=host)
+                n = len(ri.share.runs)
+                assert len(calls) == 2 * n
+                assert [c[0] for c in Fake.calls] == (["fwd_host"] * n + ["bwd_host"] * n if host
+                                                      else ["fwd"] * n + ["bwd"] * n)
+                for k, run in enumerate(ri.share.runs):
+                    for rec, buf in ((Fake.calls[k], x), (Fake.calls[n + k], g)):
+                        _, shape, ptr, cshape, st, en = rec
+                        assert shape == (run.nb, run.ns, 2, 10) and (st, en) == (3, 9)
+                        assert ptr == buf.data_ptr() + ri.share.offset(run) * 2 * 10 * 2
+                        assert cshape == (run.nb, run.ns, 1, 6)
