@@ -661,6 +661,8 @@ def odd_breakdown(device, peak, flush, l2):
         xd = synth.to_torch(x, w0.dtype).to(device)
         pos = synth.positions(w0)
         for st, en in cases:
+            if not wanted(f"{name} [{st},{en})"):
+                continue
             L = en - st
             w = dataclasses.replace(w0, start=st, end=en, r_shape=w0.r_shape[:3] + (L,))
             r1, r2 = synth.rope_table(pos, L, w.dtype)
@@ -698,6 +700,8 @@ def positions_breakdown(device, peak, flush, l2):
     out = {}
     for name, modes in (("gqa", ("interleave", "half")), ("mla_decode_q", ("interleave",)),
                         ("large_unaligned", ("interleave", "half"))):
+        if not wanted(name):
+            continue
         w = synth.WORKLOADS[name]
         x = synth.normal(w.shape, w.dtype, w.seed)
         pos = np.ascontiguousarray(synth.positions(w)[..., 0], dtype=np.int32)
@@ -719,23 +723,43 @@ def positions_breakdown(device, peak, flush, l2):
     return out
 
 
+# `--section ... --case TEXT` runs only the entries whose label holds TEXT.
+CASE = None
+
+
+def wanted(label: str) -> bool:
+    return CASE is None or CASE in label
+
+
 def half_breakdown(device, peak, flush, l2):
     """The half-split rotary mode (pairs (i, i + L/2)) on the gqa and large
-    fp32 shapes with a half-layout cos/sin table, forward, per launch."""
+    fp32 shapes with a half-layout cos/sin table, forward, per launch.  Their
+    rows are 8 and 32 accesses per half pair, so a lane's partner access
+    comes from another lane (rope_partial_half_lanes_kernel); the large
+    shape's [0, 96) has 12 per half and runs both halves in one thread
+    (rope_partial_half_kernel)."""
+    import dataclasses
     from place_partial_rope_gb300 import binding
     out = {}
-    for name in ("gqa", "large_unaligned"):
-        w = synth.WORKLOADS[name]
+    L0 = synth.WORKLOADS["large_unaligned"]
+    cases = (("gqa", synth.WORKLOADS["gqa"]), ("large_unaligned", L0),
+             ("large_unaligned [0,96)", dataclasses.replace(L0, start=0, end=96,
+                                                            r_shape=L0.r_shape[:3] + (96,))))
+    for name, w in cases:
+        if not wanted(name):
+            continue
         x = synth.normal(w.shape, w.dtype, w.seed)
         r1, r2 = synth.rope_table(synth.positions(w), w.L, w.dtype, layout="half")
         xd = synth.to_torch(x, w.dtype).to(device)
         c, s = synth.to_torch(r1, w.dtype).to(device), synth.to_torch(r2, w.dtype).to(device)
         call = binding.prepare_fwd(xd, c, s, w.start, w.end, mode="half")
+        plan = binding.rope_partial_plan(xd, c, s, w.start, w.end, 0, "half")
         for _ in range(3):
             call()
         t = time_launches(call, 50, flush)
         tb = time_back_to_back(call, 50)
-        out[name] = {"fwd": {"cold_us": round(t * 1e6, 2),
+        out[name] = {"fwd": {"kernel": "half_lanes" if plan.path == 3 else "half",
+                             "cold_us": round(t * 1e6, 2),
                              "cold_frac": round(w.algorithmic_bytes() / t / 1e9 / peak, 4),
                              "steady_us": round(tb * 1e6, 2),
                              "steady_frac": round(w.algorithmic_bytes() / tb / 1e9 / peak, 4)}}
@@ -1135,9 +1159,11 @@ SECTIONS = {
 }
 
 
-def run_section(name: str) -> int:
+def run_section(name: str, case=None) -> int:
     """One part of the breakdown on cuda:0, alone, so that a profiler sees
-    only its launches."""
+    only its launches (with `case`, only its entries whose label holds it)."""
+    global CASE
+    CASE = case
     from place_partial_rope_gb300 import build
     build.build()
     device = torch.device("cuda", 0)
@@ -1188,9 +1214,10 @@ def main():
     ap.add_argument("--section", choices=sorted(SECTIONS),
                     help="run only this part of the per-workload breakdown and print its JSON "
                          "(for profiling one kernel kind; not a bench line)")
+    ap.add_argument("--case", help="with --section: only the entries whose label holds this text")
     args = ap.parse_args()
     if args.section:
-        return run_section(args.section)
+        return run_section(args.section, args.case)
     if args.warmup < 3 and args.impl == "native":
         args.warmup = 3
     world = dist_env()[0]

@@ -926,24 +926,40 @@ __device__ __forceinline__ float two_pi_a() { return __uint_as_float(0x40c90fdbu
 __device__ __forceinline__ float two_pi_b() { return __uint_as_float(0xb43bbd2eu); }  // -1.7484555e-07
 __device__ __forceinline__ float two_pi_c() { return __uint_as_float(0xa7f72cedu); }  // -6.8604980e-15
 __device__ __forceinline__ float inv_two_pi() { return __uint_as_float(0x3e22f983u); } //  0.15915494
+// 1/(2*pi) minus inv_two_pi(), rounded to fp32 (1/(2*pi) =
+// 0.159154943091895335768883763372514362...)
+__device__ __forceinline__ float inv_two_pi_lo() { return __uint_as_float(0x31dc9c88u); } // 6.4206382e-09
 
 // cos and sin of theta = p * omega, omega = hi + lo.  theta is carried as
 // th + tl (th = p*hi rounded; tl = the exact residual of that product plus
-// p*lo), so it is accurate to about 2^-44 relative for |p| < 2^24 (p is
-// then exact in fp32).  Reduction by 2*pi follows Cody and Waite
-// ("Software Manual for the Elementary Functions", 1980) with the three-part
-// constant above: r = ((th - n*A) - n*B) - n*C + tl, where the first step is
-// exact (Sterbenz when |th| < 4, otherwise both terms are multiples of the
-// first part's ulp and the difference has at most 23 bits).  The other three
-// steps round once each, so |r - (theta - 2*pi*n)| <= 3 * 2^-23 and |r| stays
-// within pi plus a rounding.  On that range the hardware __sincosf has an
-// absolute error of at most 2^-21.41 (CUDA's documented bound for |x| <= pi),
-// so the cos/sin used are within 2^-21.41 + 3 * 2^-23 < 8e-7 of the exact
-// values, at a few instructions per angle.
+// p*lo), accurate to about 2^-44 relative for |p| < 2^24 (p is then exact in
+// fp32).  Reduction by 2*pi follows Cody and Waite ("Software Manual for the
+// Elementary Functions", 1980) with the three-part constant above.  The
+// multiple n is the integer nearest theta / (2*pi), taken from the quotient
+// as a two-part sum (the rounded product th * (1/2pi), its exact residual,
+// the constant's tail and tl's share), so that the reduced angle stays in
+// [-pi, pi] up to rounding: a plain rintf(th * (1/2pi)) can be one off when
+// |theta| is near 2^24, leaving |r| up to about 4.9, where the hardware
+// sine's error bound does not hold.  Then r = ((th - n*A) - n*B) - n*C + tl,
+// where the first step is exact (Sterbenz when |th| < 4, otherwise both
+// terms are multiples of the first part's ulp and the difference has at most
+// 23 bits).  The other three steps round once each, so |r - (theta - 2*pi*n)|
+// <= 3 * 2^-23 (an fp32 emulation of these steps over 2^24-wide position
+// ranges and bases 2 to 10^6 measured at most 2.6e-7).  On [-pi, pi] the
+// hardware __sincosf has an absolute error of at most 2^-21.41 (CUDA's
+// documented bound), so the cos/sin used are within about 7e-7 of the exact
+// values (the GPU test of this bound asserts 8e-7), at a few instructions
+// per angle.
 __device__ __forceinline__ void angle_cos_sin(float p, float w_hi, float w_lo, float& c, float& s) {
     const float th = __fmul_rn(p, w_hi);
     const float tl = __fmaf_rn(p, w_lo, __fmaf_rn(p, w_hi, -th));
-    const float n = rintf(__fmul_rn(th, inv_two_pi()));
+    const float q_hi = __fmul_rn(th, inv_two_pi());
+    float q_lo = __fmaf_rn(th, inv_two_pi(), -q_hi);
+    q_lo = __fmaf_rn(th, inv_two_pi_lo(), q_lo);
+    q_lo = __fmaf_rn(tl, inv_two_pi(), q_lo);
+    float n = rintf(q_hi);
+    const float f = __fadd_rn(__fsub_rn(q_hi, n), q_lo);  // theta / (2*pi) - n
+    n = f > 0.5f ? n + 1.0f : (f < -0.5f ? n - 1.0f : n);
     float r = __fmaf_rn(-n, two_pi_a(), th);
     r = __fmaf_rn(-n, two_pi_b(), r);
     r = __fmaf_rn(-n, two_pi_c(), r);

@@ -11,6 +11,8 @@ fp32, 1 ulp of bf16 / fp16).  In lanes where the two products cancel that
 can be several units in the last place of y, so a pure ulp bound would be
 wrong.  Every byte outside the slice is bit-exact.
 """
+import math
+
 import numpy as np
 import pytest
 import torch
@@ -86,3 +88,36 @@ def test_position_zero_is_the_identity_on_the_gpu():
     x = synth.normal((2, 3, 4, 32), "bf16", 3)
     got = run("fwd", x, np.zeros((1, 1), np.int32), "bf16", 0, 32, "interleave")
     assert np.array_equal(got, x)
+
+
+@pytest.mark.parametrize("mode", ["interleave", "half"])
+@pytest.mark.parametrize("base,L", [(10000.0, 64), (10000.0, 2), (500000.0, 128), (1e6, 512),
+                                    (2.0, 16)])
+def test_kernel_cos_sin_error_bound(base, L, mode):
+    """The premise of the bar above, measured: with unit pairs (x_m, x_n) =
+    (1, 0) the forward writes the kernel's own cos and sin (1*c - 0*s = c and
+    0*c + 1*s = s, each product and sum exact), so comparing them with the
+    fp64 cos/sin of p * base^(-2k/L) gives the kernel's angle error directly.
+    Positions span [-2^24, 2^24), where they are exact in fp32, with the
+    ends and small values included.  ("ANE实战 RoPE位置编码在MIL中的纯ANE实现",
+    sections 先搞懂RoPE and 第一步: theta_k = p / base^(2k/L).)"""
+    rng = np.random.default_rng(2024)
+    ends = np.array([0, 1, -1, 2, 3, 7, 1000, -1000, 2**23, -2**23, 2**24 - 1, -2**24,
+                     2**24 - 2, 12345678, -9876543], np.int64)
+    p = np.concatenate([ends, rng.integers(-2**24, 2**24, size=4096 - ends.size)]).astype(np.int32)
+    S = p.size
+    x = np.zeros((1, S, 1, L), np.float32)
+    if mode == "half":
+        x[..., :L // 2] = 1.0   # x_m = 1 in the first half, x_n = 0 in the second
+    else:
+        x[..., 0::2] = 1.0      # x_m = 1 in even lanes, x_n = 0 in odd lanes
+    got = run("fwd", x, p[None, :], "fp32", 0, L, mode, base).astype(np.float64)
+    k = np.arange(L // 2, dtype=np.float64)
+    theta = p.astype(np.float64)[:, None] * np.array([math.pow(base, -2.0 * kk / L) for kk in k])
+    if mode == "half":
+        c, s = got[0, :, 0, :L // 2], got[0, :, 0, L // 2:]
+    else:
+        c, s = got[0, :, 0, 0::2], got[0, :, 0, 1::2]
+    err = max(np.abs(c - np.cos(theta)).max(), np.abs(s - np.sin(theta)).max())
+    print(f"base {base} L {L} {mode}: max |cos/sin error| {err:.3e}")
+    assert err <= 8e-7, err
