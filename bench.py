@@ -87,14 +87,25 @@ def strip_c_comments(text: str) -> str:
     return " ".join("".join(out).split())
 
 
-def kernel_source_hash() -> str:
-    """Hash of the kernel sources with comments and layout removed, to tell
-    whether stored ncu counters still describe the code that runs."""
+# The files that define the kernels' device code.  The host planner and the
+# launcher are left out: they choose among the kernel instances, and a
+# traffic line names the instance it was measured on.
+KERNEL_SOURCES = ("fast_div.h", "rope_internal.h", "rope_kernels.cuh", "rope_kernels_bf16.cu",
+                  "rope_kernels_fp16.cu", "rope_kernels_fp32.cu")
+
+
+def kernel_source_hash(read=None) -> str:
+    """Hash of the kernels' device-code sources with comments and layout
+    removed, to tell whether stored ncu counters still describe the code that
+    runs.  `read(name)` returns a file's text (default: the file in CSRC)."""
     h = hashlib.sha256()
-    for f in sorted(os.listdir(CSRC)):
-        if f.endswith((".cu", ".cuh", ".h", ".cpp")):
+    for f in KERNEL_SOURCES:
+        if read is None:
             with open(os.path.join(CSRC, f), encoding="utf-8") as fh:
-                h.update(f.encode() + b"\0" + strip_c_comments(fh.read()).encode())
+                text = fh.read()
+        else:
+            text = read(f)
+        h.update(f.encode() + b"\0" + strip_c_comments(text).encode())
     return h.hexdigest()[:16]
 
 

@@ -92,7 +92,9 @@ typedef enum {
  *              Each of rX_shape[0..2] is 1 (broadcast; its stride is then
  *              ignored) or equal to B, S, N respectively; rX_shape[3] == L.
  *              rX_stride[3] must be 1 and the other strides >= 0.  r1 and r2
- *              are only read and must not overlap x.
+ *              are only read and must not overlap x: a call whose x shares a
+ *              byte with r1 or r2 (from its first element to the end of its
+ *              farthest row) returns ROPE_ERR_INVALID.
  *   B, S, N, D sizes of x, each >= 0; D even and D <= 1024.
  *   start, end 0 <= start <= end <= D and L = end - start even.  start may be
  *              odd: pairs are counted from start.
@@ -206,7 +208,8 @@ rope_status_t rope_partial_inplace_bwd_pos(void* grad, const int32_t* positions,
  *
  *   q, k       device pointers to contiguous (B, S, Nq, Dq) and (B, S, Nk, Dk)
  *              tensors of `dtype` (the key may have its own head count and
- *              head dim); both are read and written.
+ *              head dim); both are read and written, so they must not share a
+ *              byte (ROPE_ERR_INVALID), nor may either share one with r1/r2.
  *   q_start/q_end, k_start/k_end
  *              the two slices; same rules as `start`/`end` above, and the same
  *              length L = q_end - q_start = k_end - k_start.

@@ -133,19 +133,21 @@ rope_status_t check(const void* x, const void* r1, const void* r2, int dtype, in
 // accesses of the large shape's slice at byte 136 ran 99.5 us at U = 4
 // against 110.8 us at 2 and 100.4 us at 8 (the positions call: 97.1 us);
 // 16-byte accesses ran 82.7 us at U = 2 against 83.2 us at 4 ([32, 96))
-// and 159.7 against 160.0 us (the whole 512-byte row).  A thread that holds
-// both halves of a half-split pair moves two accesses per head, so it takes
-// half of that ([2, 98), 8-byte accesses: 135 us at U = 2 against 203 us at
-// 1; [1, 97), 4-byte: 156 us at U = 4 against 257 us at 1).  16-bit rows:
+// and 159.7 against 160.0 us (the whole 512-byte row).  16-bit rows:
 // 16-byte accesses want 4 (gqa 42.0 us; flat from 2 to 8 on 256-byte rows,
 // best at 4 on 384-byte rows), 8-byte ones 2 (55.5 us against 57.7 at 4)
 // and 4-byte ones 4 (57.5 us against 71.9 at 2).  The half-split kernel that
 // takes its partner from another lane wants more in flight (8-byte accesses
 // 56.5 us at U = 4 against 57.4 at 2; 4-byte ones 57.4 us at 8 against 59.6
-// at 4).  With both halves in one thread 16-bit rows want 4 for 16-byte
-// accesses ([0, 48): 45.2 us against 49.4 at 2) and 2 otherwise, except the
-// positions call, which wants 2 (gqa 44.8 us against 47.4 at 4).  The
-// element path is best at 8 (4 with both halves in one thread).
+// at 4).  The half-split kernel with both halves in one thread (table call,
+// on the full grid): fp32 2 on 16- and 8-byte accesses ([0, 96) 118.9 us
+// against 148.9 at 1 and 119.5 at 4; [2, 98) 133.0 against 153.3 at 1) and
+// 8 on 4-byte ones ([1, 97) 152.2 against 154.7 at 4); 16-bit 4 on 16-byte
+// accesses (gqa shape [0, 96) 61.3 us against 69.2 at 1; [0, 48) 38.7
+// against 37.8 at 1 and 45.7 at 2) and 8 on 8- and 4-byte ones ([4, 52)
+// 36.6 against 38.8 at 2; [2, 50) 39.3 against 41.6 at 2).  The positions
+// call with both halves in one thread wants 2 (gqa 44.8 us against 47.4 at
+// 4).  The element path is best at 8 (4 with both halves in one thread).
 // The odd-start kernel (a lane per aligned vector of x, vec bytes): 4 heads
 // per thread on 16-byte vectors (the most that kernel instance allows), 8
 // on 8-byte ones.  Back to back on GB300: GQA [1, 65) 16-byte 58.0 us (U
@@ -161,10 +163,11 @@ int heads_cap(int e, int vec, int path, bool pair, bool lanes, bool pos) {
     if (path == kScalarPair) return pair ? 4 : 8;
     if (path == kOddPair) return odd_heads_cap(e, vec);
     if (e == 4) {
+        if (pair && !pos) return vec == 4 ? 8 : 2;
         const int per_head = pair ? 2 * vec : vec;  // bytes of x per head
         return per_head >= 32 ? 1 : 32 / per_head;
     }
-    if (pair) return (vec == 16 && !pos) ? 4 : 2;
+    if (pair) return pos ? 2 : (vec == 16 ? 4 : 8);
     if (lanes) return vec == 16 ? 4 : (vec == 8 ? 4 : 8);
     return vec == 8 ? 2 : 4;
 }
@@ -291,22 +294,20 @@ rope_status_t make_plan(int dir, int mode, int dtype, const Seg* seg, int nseg, 
     const bool pair = half && !P->lanes;
     P->U = choose_heads_per_thread(seg[0].N,
                                    host ? 1 : heads_cap(e, P->vec, P->path, pair, P->lanes, pos));
-    // Grid: for one tensor, a grid of one block per 256 work items, whose
-    // blocks the hardware replaces as they finish, ran faster than a
-    // resident grid whose threads stride over the work (the large fp32
-    // shape 99.5 against 103.2 us, its positions call 97.1 against 103.9 us,
-    // [32, 96) 82.7 against 86.9 us; gqa 42.0 against 44.7 us; the 16-bit
-    // element path in half-split mode 75.8 against 83.8 us; the fused query
-    // + key call, whose work index sweeps the query, then the key, 47.3
-    // against 51.2 us cold on a GQA pair).  The exceptions ran faster on the
-    // resident grid: 16-bit rows read over the host link (mla_decode_q
-    // 422 against 441 us; gqa level at 815-819 us, while the large fp32
-    // shape there ran 2184 against 2291 us on the full grid), and the table
-    // call's half-split kernel with both halves in one thread when an access
-    // holds more than two elements ([0, 96) fp32: 144 against 150 us; [0, 48)
-    // fp16: 45.2 against 47.4 us; [4, 52) fp16: 40.2 against 41.3 us).
-    const bool wide_pair = pair && !pos && P->path == kVector && P->vec / e > 2;
-    P->full_grid = host ? (e == 4 && nseg == 1) : !wide_pair;
+    // Grid: a grid of one block per 256 work items, whose blocks the
+    // hardware replaces as they finish, ran faster than a resident grid whose
+    // threads stride over the work (the large fp32 shape 99.5 against 103.2
+    // us, its positions call 97.1 against 103.9 us, [32, 96) 82.7 against
+    // 86.9 us; gqa 42.0 against 44.7 us; the 16-bit element path in
+    // half-split mode 75.8 against 83.8 us; the half-split kernel with both
+    // halves in one thread, [0, 96) fp32 118.9 against 155.5 us at U = 2,
+    // gqa shape [0, 96) 61.3 against 68.4 us at U = 4; the fused query + key
+    // call, whose work index sweeps the query, then the key, 47.3 against
+    // 51.2 us cold on a GQA pair).  The exception ran faster on the resident
+    // grid: 16-bit rows read over the host link (mla_decode_q 422 against
+    // 441 us; gqa level at 815-819 us, while the large fp32 shape there ran
+    // 2184 against 2291 us on the full grid).
+    P->full_grid = host ? (e == 4 && nseg == 1) : true;
     // head groups of each tensor (the fused call sweeps the first tensor's
     // items, then the second's)
     const int64_t H = (seg[0].N + P->U - 1) / P->U;
@@ -397,6 +398,25 @@ int64_t r_extent(const Resolved& R, int r, const int64_t* shape) {
     return far + R.L * R.e;
 }
 
+// Byte ranges [a, a + na) and [b, b + nb) share a byte.
+bool overlaps(const void* a, int64_t na, const void* b, int64_t nb) {
+    const uintptr_t pa = reinterpret_cast<uintptr_t>(a), pb = reinterpret_cast<uintptr_t>(b);
+    return na > 0 && nb > 0 && pa < pb + uint64_t(nb) && pb < pa + uint64_t(na);
+}
+
+// x (or a gradient) is written in place while r1 and r2 are read: they must
+// not share bytes (a tensor's bytes: x whole, cos/sin from their first to
+// the end of their farthest row).
+rope_status_t check_disjoint(const char* what, const void* x, int64_t xbytes, const void* r1,
+                             const void* r2, const Resolved& R, const int64_t* r1_shape,
+                             const int64_t* r2_shape) {
+    if (overlaps(x, xbytes, r1, r_extent(R, 0, r1_shape)))
+        return fail(ROPE_ERR_INVALID, "r1 (cos) overlaps %s, which is written in place", what);
+    if (overlaps(x, xbytes, r2, r_extent(R, 1, r2_shape)))
+        return fail(ROPE_ERR_INVALID, "r2 (sin) overlaps %s, which is written in place", what);
+    return ROPE_OK;
+}
+
 // Plan, size and launch every piece of a validated call.
 // The positions call's extra state: where the positions are and the
 // frequency table.
@@ -459,6 +479,8 @@ rope_status_t run(int dir, void* x, const void* r1, const void* r2, int dtype, i
     rope_status_t st = check(x, r1, r2, dtype, B, S, N, D, r1_shape, r1_stride, r2_shape,
                              r2_stride, start, end, &R);
     if (st != ROPE_OK || R.empty) return st;
+    st = check_disjoint("x", x, B * S * N * D * R.e, r1, r2, R, r1_shape, r2_shape);
+    if (st != ROPE_OK) return st;
     if (host_buffers) {
         // the kernel works on the host buffers in place: take the addresses
         // the device uses for them, or refuse a buffer it cannot reach
@@ -499,6 +521,16 @@ rope_status_t run_qk(int dir, void* q, void* k, const void* r1, const void* r2, 
     st = check(k, r1, r2, dtype, B, S, Nk, Dk, r1_shape, r1_stride, r2_shape, r2_stride, k_start,
                k_end, &Rk);
     if (st != ROPE_OK) return fail_prefixed(st, "key");
+    // q and k are both written: they must not share a byte, nor may either
+    // share one with r1 / r2
+    const int64_t qbytes = Rq.empty ? 0 : B * S * Nq * Dq * Rq.e;
+    const int64_t kbytes = Rk.empty ? 0 : B * S * Nk * Dk * Rk.e;
+    if (overlaps(q, qbytes, k, kbytes))
+        return fail(ROPE_ERR_INVALID, "query and key overlap; both are written in place");
+    if (!Rq.empty && (st = check_disjoint("the query", q, qbytes, r1, r2, Rq, r1_shape, r2_shape)) != ROPE_OK)
+        return st;
+    if (!Rk.empty && (st = check_disjoint("the key", k, kbytes, r1, r2, Rk, r1_shape, r2_shape)) != ROPE_OK)
+        return st;
     Seg seg[2];
     int nseg = 0;
     if (!Rq.empty) seg[nseg++] = Seg{q, Nq, Dq, q_start};

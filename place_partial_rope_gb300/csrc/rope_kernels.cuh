@@ -47,7 +47,10 @@
 //   * launches use programmatic dependent launch: every kernel waits on
 //     griddepcontrol before its first global access, so only its launch and
 //     ramp overlap the tail of the kernel before it in the stream.
-// Only slice bytes are read or written; every other byte of x is untouched.
+// Only slice bytes are written; every other byte of x is left as it was.
+// Reads stay inside each row: the odd-start kernel also reads the elements
+// of its edge vectors outside the slice (at least element start - 1 and the
+// word that holds element end); the other kernels read only slice bytes.
 #pragma once
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>

@@ -228,7 +228,7 @@ def test_heads_per_thread(lib, N, vec, U):
     (34, 98, 1, 8, 4),     # 8-byte accesses
     (1, 65, 1, 16, 4),     # odd start: a lane per aligned 16-byte vector (4 heads)
     (34, 98, 2, 8, 4),     # half-split, partner in another lane (32 accesses per row)
-    (0, 96, 2, 16, 1),     # half-split, 48 lanes per half = 12 accesses: both halves in one thread
+    (0, 96, 2, 16, 2),     # half-split, 48 lanes per half = 12 accesses: both halves in one thread
     (2, 98, 2, 8, 2),      # 24 accesses per half of 8 bytes: both halves in one thread
 ])
 def test_heads_per_thread_fp32(lib, start, end, mode, vec, U):
@@ -311,6 +311,34 @@ def test_qk_rejected_calls(lib, fn, kwargs, status, needle):
     assert needle in lib.rope_last_error_message().decode()
 
 
+@pytest.mark.parametrize("fn", ALL_FNS)
+@pytest.mark.parametrize("kwargs,needle", [
+    (dict(r1=BASE + 16), "r1 (cos) overlaps x"),             # cos inside x
+    (dict(r2=BASE + 766), "r2 (sin) overlaps x"),            # sin's first bytes on x's last
+    (dict(r1=BASE - 62), "r1 (cos) overlaps x"),             # cos's last row runs into x
+])
+def test_cos_sin_overlapping_x_are_rejected(lib, fn, kwargs, needle):
+    """x is written in place while r1 and r2 are read, so a call whose x
+    shares a byte with either is refused before any CUDA call (x here is
+    2*4*3*16 fp16 = 768 bytes; cos/sin (1, 4, 1, 8) span 64 bytes)."""
+    st = call(lib, fn, **kwargs)
+    assert st == INVALID, (st, lib.rope_last_error_message())
+    assert needle in lib.rope_last_error_message().decode()
+
+
+@pytest.mark.parametrize("fn", ["rope_partial_inplace_fwd_qk", "rope_partial_inplace_bwd_qk"])
+@pytest.mark.parametrize("kwargs,needle", [
+    (dict(k=BASE + 4 * 8 * 192 * 2 - 2), "query and key overlap"),   # key starts on q's last element
+    (dict(k=BASE + 64), "query and key overlap"),
+    (dict(r1=BASE + 2**32 + 32), "overlaps the key"),
+    (dict(r2=BASE + 1024), "overlaps the query"),
+])
+def test_qk_overlapping_tensors_are_rejected(lib, fn, kwargs, needle):
+    st = qk_call(lib, fn, **kwargs)
+    assert st == INVALID, (st, lib.rope_last_error_message())
+    assert needle in lib.rope_last_error_message().decode()
+
+
 def test_qk_empty_calls(lib):
     assert qk_call(lib, qs=0, qe=0, ks=5, ke=5, q=0, k=0, r1=0, r2=0) == OK   # empty slices
     assert qk_call(lib, B=0, q=0, k=0, r1=0, r2=0, r_shape=(1, 1, 1, 64)) == OK
@@ -356,12 +384,12 @@ def test_half_split_plans(lib):
     # 64 accesses of the first half
     st, p = plan_mode(lib, HALF, dtype=FP32, shape=(2, 4, 3, 512), start=0, end=512)
     assert st == OK and (p.path, p.vec_bytes, p.chunks_per_row) == (1, 16, 64)
-    # both halves in one thread with accesses of more than two elements:
-    # the resident grid (8 blocks per SM on 152 SMs); of two or fewer, one
-    # block per 256 work items
+    # both halves in one thread: one block per 256 work items, 2 heads per
+    # thread for fp32 16- and 8-byte accesses
     st, p = plan_mode(lib, HALF, dtype=FP32, shape=(4, 8192, 32, 128), start=0, end=96,
                       r_shape=(4, 8192, 1, 96))
-    assert st == OK and (p.path, p.vec_bytes, p.heads_per_thread, p.blocks) == (1, 16, 1, 152 * 8)
+    assert st == OK and (p.path, p.vec_bytes, p.heads_per_thread) == (1, 16, 2)
+    assert p.blocks == p.tasks // 256
     st, p = plan_mode(lib, HALF, dtype=FP32, shape=(4, 8192, 32, 128), start=2, end=98,
                       r_shape=(4, 8192, 1, 96))
     assert st == OK and (p.path, p.vec_bytes, p.heads_per_thread) == (1, 8, 2)

@@ -269,3 +269,27 @@ def test_calls_split_into_several_launches(shape, launches):
         assert_same(rows_out, oracle.fwd(rows_in, c_h, s_h, "fp16", 0, 2), "fp16", f"rows at {t0}")
     del x, x2, ref
     torch.cuda.empty_cache()
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "fp32"])
+def test_tables_packed_right_after_x(dtype):
+    """x, cos and sin packed back to back in one allocation (adjacent byte
+    ranges that do not overlap) are accepted and rotate as separate tensors
+    would; the overlap rule refuses only shared bytes."""
+    shape, st, en = (2, 5, 3, 32), 2, 30
+    x, r1, r2, g = synth.case(shape, st, en, dtype, "BS1D", seed=21)
+    td = synth.TORCH_DTYPE[dtype]
+    n, m = x.size, r1.size
+    buf = torch.empty(n + 2 * m, dtype=td, device=DEV)
+    xv, cv, sv = buf[:n].view(shape), buf[n:n + m].view(r1.shape), buf[n + m:].view(r2.shape)
+    cv.copy_(synth.to_torch(r1, dtype).to(DEV))
+    sv.copy_(synth.to_torch(r2, dtype).to(DEV))
+    for direction, inp in (("fwd", x), ("bwd", g)):
+        xv.copy_(synth.to_torch(inp, dtype).to(DEV))
+        fn = binding.rope_partial_inplace_fwd if direction == "fwd" else binding.rope_partial_inplace_bwd
+        fn(xv, cv, sv, st, en)
+        torch.cuda.synchronize()
+        assert_same(synth.from_torch(xv), run_oracle(direction, inp, r1, r2, dtype, st, en), dtype,
+                    f"packed {direction}")
+        assert np.array_equal(synth.from_torch(cv).view(np.uint8), r1.view(np.uint8))
+        assert np.array_equal(synth.from_torch(sv).view(np.uint8), r2.view(np.uint8))
