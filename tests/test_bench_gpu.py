@@ -39,3 +39,16 @@ def test_bench_line_keeps_the_contract():
     assert out["gpu_launches"] == 2 * 5  # forward and backward per step, one launch each
     clocks = out["clocks"]
     assert clocks["sm_max_mhz"] > 0 and isinstance(clocks["reasons"], list)
+    # several timed regions of K steps; value and ms_per_step from the median
+    reg = out["timed_regions"]
+    assert reg["count"] >= 5 and reg["steps_each"] == 5
+    assert reg["min_ms"] <= reg["median_ms"] <= reg["max_ms"]
+    assert abs(out["ms_per_step"] - reg["median_ms"] / 5) < 1e-3
+    # the token split at one rank is the named workload, one run
+    assert out["config"]["split"]["mode"] == "tokens" and out["plan"]["runs_per_direction"] == 1
+    assert 0 < roof["frac_of_nominal"] < roof["frac"]
+    # per-workload entries name their figure of record; notes explain the labels
+    wl = out["workloads"]
+    assert wl["gqa"]["fwd"]["of_record"] == "steady_frac" and "notes" in wl
+    assert wl["small_model"]["fwd"]["graph_l2_resident"] is True
+    assert wl["e2e_gqa"]["value"] > 0 and wl["e2e_gqa"]["host_link"]["both_GB/s"] > 0
