@@ -949,7 +949,7 @@ def gpu_arm(args):
     _, total_elems = reduce_timing(0.0, float(ndir * share.tokens * w.shape[2] * w.L * K), world,
                                    device)
     med = statistics.median(reg_max)
-    value = total_bytes / med / 1e9
+    value = total_bytes / med / 1e9 if med > 0 else 0.0
     regions = {"count": nreg, "steps_each": K, "median_ms": round(med * 1e3, 4),
                "min_ms": round(min(reg_max) * 1e3, 4), "max_ms": round(max(reg_max) * 1e3, 4),
                "spread": round((max(reg_max) - min(reg_max)) / med, 4),
@@ -977,7 +977,7 @@ def gpu_arm(args):
     dom = max(range(ndir), key=lambda j: isolated[j])
     kname = kernel_name(plan, w.dtype, dom) if plan is not None else None
     avg = med / (ndir * K)
-    achieved = per_launch / avg / 1e9 if per_launch else 0.0
+    achieved = per_launch / avg / 1e9 if (per_launch and avg > 0) else 0.0
     traffic = stored_traffic(kname, w.name) if (kname and world == 1) else None
     floor = dram_floor_bytes(w)
     roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
@@ -1030,7 +1030,7 @@ def gpu_arm(args):
                    "at the workload's seeded positions",
            "config": config,
            "frac_of_peak": round(value / world / peak, 4),
-           "gelem_per_s": round(total_elems / med / 1e9, 2),
+           "gelem_per_s": round(total_elems / med / 1e9, 2) if med > 0 else 0.0,
            "roofline": roofline, "e2e": e2e,
            "gpu_launches": K * launches_step,
            "timed_regions": regions,
@@ -1112,7 +1112,7 @@ def e2e_measure(w, ri, device, steps: int, binding, shard, world: int = 1):
         b.record()
         torch.cuda.synchronize(device)
         t, total = reduce_timing(a.elapsed_time(b) / 1e3, algo * steps, world, device)
-        return t / steps, total / t / 1e9
+        return t / steps, (total / t / 1e9 if t > 0 else 0.0)
 
     zc = rank_calls(binding, shard, ri, {"fwd": hx, "bwd": hg}, htabs, w, host=True)
 

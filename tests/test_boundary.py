@@ -250,6 +250,9 @@ def test_huge_calls_split_into_launches(lib):
     assert p.launches == 6
     p = plan(lib, shape=(2**20, 2**11, 1, 2), start=0, end=2, r_shape=(1, 2**11, 1, 2))
     assert p.launches == 1                                           # exactly 2^31 items
+    # the odd-start kernel (one lane per row for 4 pairs) splits the same way
+    p = plan(lib, shape=(2, 2**30 + 3, 1, 16), start=1, end=9, r_shape=(1, 2**30 + 3, 1, 8))
+    assert (p.path, p.launches, p.tasks) == (4, 2, 2 * (2**30 + 3))
 
 
 def test_fast_division_exhaustive_sample(tmp_path):
