@@ -148,6 +148,14 @@ rope_status_t check(const void* x, const void* r1, const void* r2, int dtype, in
 // 36.6 against 38.8 at 2; [2, 50) 39.3 against 41.6 at 2).  The positions
 // call with both halves in one thread wants 2 (gqa 44.8 us against 47.4 at
 // 4).  The element path is best at 8 (4 with both halves in one thread).
+// Short 16-bit slices of 16-byte accesses want fewer heads: on the gqa shape
+// [0, 16) (2 accesses per row) ran 23.8 us at U = 1 against 32.7 at 4
+// (half-split 24.8 against 31.2), and 4-access slices 25.2 us at U = 2
+// against 27.7 at 4 ([0, 32), [32, 64), [64, 96); [16, 48) 32.7 against
+// 35.7); from 6 accesses on 4 stays best ([0, 48) 36.4 us), and so it does
+// for half-split rows of 4 accesses ([0, 32) 27.2 against 28.2 at 2).  (On
+// the MLA-decode shape, whose short slices stay in L2 back to back, U = 4
+// ran those 8 % faster there and level after an L2 flush.)
 // The odd-start kernel (a lane per aligned vector of x, vec bytes): 4 heads
 // per thread on 16-byte vectors (the most that kernel instance allows), 8
 // on 8-byte ones.  Back to back on GB300: GQA [1, 65) 16-byte 58.0 us (U
@@ -159,7 +167,7 @@ int odd_heads_cap(int e, int vec) {
     return vec == 16 ? 4 : 8;
 }
 
-int heads_cap(int e, int vec, int path, bool pair, bool lanes, bool pos) {
+int heads_cap(int e, int vec, int path, bool pair, bool lanes, bool pos, int chunks) {
     if (path == kScalarPair) return pair ? 4 : 8;
     if (path == kOddPair) return odd_heads_cap(e, vec);
     if (e == 4) {
@@ -168,6 +176,11 @@ int heads_cap(int e, int vec, int path, bool pair, bool lanes, bool pos) {
         return per_head >= 32 ? 1 : 32 / per_head;
     }
     if (pair) return pos ? 2 : (vec == 16 ? 4 : 8);
+    // 16-byte accesses of a short 16-bit row slice: one head per thread for
+    // 2 accesses per row (interleave or half-split lanes), two for 4
+    // (interleave)
+    if (vec == 16 && chunks <= 2) return 1;
+    if (vec == 16 && chunks <= 4 && !lanes) return 2;
     if (lanes) return vec == 16 ? 4 : (vec == 8 ? 4 : 8);
     return vec == 8 ? 2 : 4;
 }
@@ -293,7 +306,7 @@ rope_status_t make_plan(int dir, int mode, int dtype, const Seg* seg, int nseg, 
     // large fp32 shape 2.18 ms against 2.26-2.30 ms with 2 or 4.
     const bool pair = half && !P->lanes;
     P->U = choose_heads_per_thread(seg[0].N,
-                                   host ? 1 : heads_cap(e, P->vec, P->path, pair, P->lanes, pos));
+                                   host ? 1 : heads_cap(e, P->vec, P->path, pair, P->lanes, pos, P->C));
     // Grid: a grid of one block per 256 work items, whose blocks the
     // hardware replaces as they finish, ran faster than a resident grid whose
     // threads stride over the work (the large fp32 shape 99.5 against 103.2

@@ -219,8 +219,21 @@ def test_heads_per_thread(lib, N, vec, U):
     """16-bit rows: up to 4 heads per thread for 16-byte chunks, 2 for 8-byte
     chunks, never more than a quarter of the head slots idle."""
     start = 0 if vec == 16 else 4  # 8-byte slice offset forces 8-byte accesses for fp16
-    p = plan(lib, shape=(1, 2, N, 24), start=start, end=start + 8, r_shape=(1, 2, 1, 8))
+    p = plan(lib, shape=(1, 2, N, 64), start=start, end=start + 48, r_shape=(1, 2, 1, 48))
     assert p.vec_bytes == vec and p.heads_per_thread == U
+
+
+@pytest.mark.parametrize("start,end,chunks,U", [(0, 16, 2, 1), (0, 32, 4, 2), (16, 48, 4, 2),
+                                                (0, 48, 6, 4), (0, 64, 8, 4)])
+def test_heads_per_thread_short_16bit_slices(lib, start, end, chunks, U):
+    """16-byte accesses of a short 16-bit slice: one head per thread for 2
+    accesses per row, two for 4, four from 6 on; half-split rows whose
+    accesses fit a warp take one for 2 and four otherwise."""
+    p = plan(lib, shape=(32, 64, 16, 128), start=start, end=end, r_shape=(1, 64, 1, end - start))
+    assert (p.vec_bytes, p.chunks_per_row, p.heads_per_thread) == (16, chunks, U)
+    st, p = plan_mode(lib, 2, shape=(32, 64, 16, 128), start=start, end=end,
+                      r_shape=(1, 64, 1, end - start))
+    assert st == OK and p.heads_per_thread == (1 if chunks <= 2 else 4)
 
 
 @pytest.mark.parametrize("start,end,mode,vec,U", [
