@@ -326,8 +326,9 @@ const char* rope_last_error_message(void);
 typedef struct {
     int32_t path;             /* 0: no launch (empty), 1: vector kernel, 2: scalar-pair kernel, */
                               /* 3: half-split vector kernel whose row of accesses fits one     */
-                              /* warp (the partner access comes from another lane), 4: 16-bit   */
-                              /* interleave with an odd start, a lane per aligned word of x     */
+                              /* warp (the partner access comes from another lane), 4:          */
+                              /* interleave with an odd start at element 1 of an aligned        */
+                              /* vector, a lane per 16- or 8-byte vector of x                   */
     int32_t vec_bytes;        /* bytes per global access of x (16, 8 or 4; on the scalar path  */
                               /* a pair (interleave) or an element (half-split))                */
     int32_t heads_per_thread; /* heads one thread walks with its cos/sin kept in registers     */

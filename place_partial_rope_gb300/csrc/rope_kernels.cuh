@@ -6,8 +6,9 @@
 //                            warp: the partner access comes by warp shuffle
 //   rope_partial_qk_kernel   query and key in one launch, one cos/sin row
 //   rope_partial_pos_kernel  cos/sin computed from positions (no table)
-//   rope_partial_odd_kernel  16-bit interleave with an odd start: a lane
-//                            per aligned word, straddling halves by shuffle
+//   rope_partial_odd_kernel  interleave with an odd start at element 1 of an
+//                            aligned 16- or 8-byte vector: a lane per
+//                            vector, the straddling elements by shuffle
 //
 // What it computes ("CANN ops-transformer inplace_partial_rotary_mul",
 // section 功能与计算公式, and its kernel op chain): for every row
@@ -30,9 +31,10 @@
 //     with one access per element ("scalar pair"); in half-split mode a
 //     chunk's partner lies L/2 lanes on: in another lane of the warp when
 //     the row's chunks fit one warp (a shuffle brings it), otherwise in the
-//     same thread; a 16-bit slice with an odd start has its pairs straddle
-//     aligned words, and rows of up to 32 pairs then take a lane per word
-//     with the straddling halves brought by shuffle;
+//     same thread; with an odd start every pair straddles two aligned
+//     accesses, and a slice that starts at element 1 of an aligned vector
+//     takes a lane per vector with the straddling elements brought by
+//     shuffle;
 //   * a thread keeps the chunk's cos/sin in registers and walks U
 //     consecutive heads of the same token (heads hg*U .. hg*U + U - 1),
 //     issuing all U loads of x before any arithmetic, so U accesses per
@@ -40,10 +42,10 @@
 //   * consecutive threads take consecutive chunks of a row, so a warp reads
 //     whole 32-byte sectors of each row's slice;
 //   * the flat work index is split by three multiply-high divisions per
-//     item; the grid usually covers it once (one block per 256 items, so
-//     the hardware starts a block as each one ends), and for the cases that
-//     measured faster that way it is sized to the resident blocks of all
-//     SMs and strides over the work (the host picks per access kind);
+//     item; the grid covers it once (one block per 256 items, so the
+//     hardware starts a block as each one ends), except for 16-bit rows read
+//     over the host link, where a grid of the resident blocks of all SMs
+//     strides over the work (the host picks; both measured);
 //   * launches use programmatic dependent launch: every kernel waits on
 //     griddepcontrol before its first global access, so only its launch and
 //     ramp overlap the tail of the kernel before it in the stream.
