@@ -146,8 +146,13 @@ rope_status_t check(const void* x, const void* r1, const void* r2, int dtype, in
 // accesses (gqa shape [0, 96) 61.3 us against 69.2 at 1; [0, 48) 38.7
 // against 37.8 at 1 and 45.7 at 2) and 8 on 8- and 4-byte ones ([4, 52)
 // 36.6 against 38.8 at 2; [2, 50) 39.3 against 41.6 at 2).  The positions
-// call with both halves in one thread wants 2 (gqa 44.8 us against 47.4 at
-// 4).  The element path is best at 8 (4 with both halves in one thread).
+// call computes each thread's angles once for all its heads, so it wants
+// more of them: fp32 4 on 16- and 8-byte accesses ([32, 96) 78.5 us
+// against 88.3 at 2), 2 with both halves in one thread on 16-byte ones
+// ([0, 96) 115.8 against 134.0 at 1); 16-bit 4 on 8-byte accesses ([4, 68)
+// 54.7 against 58.6 at 2) and 8 on 4-byte ones ([2, 66) 54.7 against 59.5
+// at 4), 2 with both halves in one thread (gqa 44.8 us against 47.4 at 4).
+// The element path is best at 8 (4 with both halves in one thread).
 // Short 16-bit slices of 16-byte accesses want fewer heads: on the gqa shape
 // [0, 16) (2 accesses per row) ran 23.8 us at U = 1 against 32.7 at 4
 // (half-split 24.8 against 31.2), and 4-access slices 25.2 us at U = 2
@@ -171,9 +176,9 @@ int heads_cap(int e, int vec, int path, bool pair, bool lanes, bool pos, int chu
     if (path == kScalarPair) return pair ? 4 : 8;
     if (path == kOddPair) return odd_heads_cap(e, vec);
     if (e == 4) {
-        if (pair && !pos) return vec == 4 ? 8 : 2;
-        const int per_head = pair ? 2 * vec : vec;  // bytes of x per head
-        return per_head >= 32 ? 1 : 32 / per_head;
+        if (pair) return vec == 4 ? (pos ? 4 : 8) : 2;
+        if (pos) return 4;
+        return vec >= 32 ? 1 : 32 / vec;  // about 32 bytes of x per thread
     }
     if (pair) return pos ? 2 : (vec == 16 ? 4 : 8);
     // 16-byte accesses of a short 16-bit row slice: one head per thread for
@@ -182,6 +187,7 @@ int heads_cap(int e, int vec, int path, bool pair, bool lanes, bool pos, int chu
     if (vec == 16 && chunks <= 2) return 1;
     if (vec == 16 && chunks <= 4 && !lanes) return 2;
     if (lanes) return vec == 16 ? 4 : (vec == 8 ? 4 : 8);
+    if (pos) return vec == 4 ? 8 : 4;
     return vec == 8 ? 2 : 4;
 }
 
