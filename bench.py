@@ -656,17 +656,19 @@ def e2e_aligned(device) -> dict:
 def odd_breakdown(device, peak, flush, l2):
     """Odd slice starts, forward, per launch: on the gqa shape (fp16, one
     cos/sin row per position) [1, 65) (32 pairs per row), [1, 63) (31: the
-    row's last lane stores part of its vector) and [3, 45) (21 pairs from
-    element 3 of a vector); on the large fp32 shape (per-batch position
-    offsets) [1, 65).  A start at element 1 of a 16-byte vector runs the
-    odd-start kernel (path 4, a lane per aligned vector of x), [3, 45) the
-    element path (path 2).  Such a slice touches one more 64-byte DRAM atom
-    per row than an aligned one, so each entry also gives the layout's DRAM
-    floor and the fraction of it."""
+    row's last lane stores part of its vector), [5, 69) (element 1 of an
+    8-byte vector) and [3, 45) (21 pairs from element 3 of a vector); on the
+    large fp32 shape (per-batch position offsets) [1, 65) and [3, 67).  A
+    start at element 1 of a 16- or 8-byte vector runs the odd-start kernel
+    (path 4, a lane per aligned vector of x), [3, 45) the element path
+    (path 2).  Such a slice touches one more 64-byte DRAM atom per row than
+    an aligned one, so each entry also gives the layout's DRAM floor and the
+    fraction of it."""
     import dataclasses
     from place_partial_rope_gb300 import binding
     out = {}
-    for name, cases in (("gqa", ((1, 65), (1, 63), (3, 45))), ("large_unaligned", ((1, 65),))):
+    for name, cases in (("gqa", ((1, 65), (1, 63), (5, 69), (3, 45))),
+                        ("large_unaligned", ((1, 65), (3, 67)))):
         w0 = synth.WORKLOADS[name]
         x = synth.normal(w0.shape, w0.dtype, w0.seed)
         xd = synth.to_torch(x, w0.dtype).to(device)

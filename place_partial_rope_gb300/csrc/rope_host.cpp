@@ -238,21 +238,21 @@ rope_status_t make_plan(int dir, int mode, int dtype, const Seg* seg, int nseg, 
     P->half = half;
     // Interleave with an odd start (one tensor, table call): every pair
     // straddles two aligned accesses.  A lane per aligned V-byte vector of x,
-    // V the widest of 16 and 8 bytes that divides x's address and its row
-    // pitch, when the slice starts at element 1 of its vector (start = 1
-    // modulo V / e; then each lane's cos/sin are the pair-aligned V bytes at
-    // its own offset): cos/sin are loaded a pair at a time (a 4-byte word per
-    // 16-bit pair, two per fp32 pair, so their rows must be 4-byte aligned),
-    // or one V-byte access per lane when their rows are V-aligned.  A lane's
-    // vector holds VE = V / e elements and the first elements of PV = VE / 2
-    // pairs, so a row takes (P - 1) / PV + 1 lanes for its P pairs.  Other
-    // odd starts run the element path, which measured faster there (back to
-    // back on GB300, GQA shape: [3, 45) 48.5 against 50.7 us; 16-bit rows only
-    // 4-byte aligned, [1, 65): 74.0 against 78.6 us; large fp32 [3, 67): 108.2
-    // against 109.6 us), while this kernel wins at [1, 65) (58.5 against
-    // 74.1 us), [1, 63) (53.9 against 58.6), the MLA-decode query's [1, 65)
-    // (32.1 against 43.0) and the large fp32 shape's [1, 65) (98.9 against
-    // 108.2).
+    // V the wider of 16 and 8 bytes that divides x's address and its row
+    // pitch and puts the start at element 1 of a vector (start = 1 modulo
+    // V / e; at 8 bytes that is any odd start for fp32, and starts = 1 or 5
+    // modulo 8 for 16-bit types).  cos/sin are loaded a pair at a time (a
+    // 4-byte word per 16-bit pair, two per fp32 pair, so their rows must be
+    // 4-byte aligned), or one V-byte access per lane when their rows are
+    // V-aligned.  A lane's vector holds VE = V / e elements and the first
+    // elements of PV = VE / 2 pairs, so a row takes (P - 1) / PV + 1 lanes for
+    // its P pairs.  Back to back on GB300 against the element path (device
+    // time, steady): GQA [1, 65) 57.0 against 73.4 us, [1, 63) 52.1 against
+    // 58.0, [5, 69) at 8 bytes 58.3 against 73.3, [13, 71) 67.4 against 84.4,
+    // x 8 bytes off 16 at [1, 65) 58.2 against 73.3; the MLA-decode query's
+    // [1, 65) 31.5 against 43.1; large fp32 [1, 65) 98.7 against 108.0 and, at
+    // 8 bytes, [3, 67) 102.8 against 108.2.  Other odd starts (16-bit starts
+    // = 3 modulo 4, rows only 4-byte aligned) run the element path.
     const int64_t pairs = R.L / 2;
     int odd_v = 0;
     if (!vec && !half && !pos && nseg == 1 && (seg[0].start & 1)) {
@@ -261,13 +261,13 @@ rope_status_t make_plan(int dir, int mode, int dtype, const Seg* seg, int nseg, 
             for (int k = 0; k < 3; ++k) r4 = r4 && R.rb[r][k] % 4 == 0;
         const uintptr_t px = reinterpret_cast<uintptr_t>(seg[0].x);
         const int64_t row = seg[0].D * e;
+        // the widest vector that x's address and row pitch allow and that
+        // puts the start at element 1 of a vector
         for (int v = 16; r4 && v >= 8; v /= 2)
-            if (px % v == 0 && row % v == 0) {
+            if (px % v == 0 && row % v == 0 && seg[0].start % (v / e) == 1) {
                 odd_v = v;
                 break;
             }
-        // the slice must start at element 1 of its vector
-        if (odd_v && seg[0].start % (odd_v / e) != 1) odd_v = 0;
     }
     P->odd_wide = false;
     if (vec) {

@@ -193,13 +193,17 @@ def test_path_choice(lib):
     assert (p.path, p.vec_bytes, p.chunks_per_row) == (ODD, 16, 2)
     p = plan(lib, dtype=FP32, start=1, end=9, x=BASE + 8)             # fp32: 1 pair per lane
     assert (p.path, p.vec_bytes, p.chunks_per_row) == (ODD, 8, 4)
+    # no 16-byte vector starts at element 1, an 8-byte one does
+    p = plan(lib, start=5, end=13)                                    # element 5 of 8, 1 of 4
+    assert (p.path, p.vec_bytes, p.chunks_per_row) == (ODD, 8, 2)
+    p = plan(lib, dtype=FP32, start=3, end=11)                        # fp32: any odd start at 8 bytes
+    assert (p.path, p.vec_bytes, p.chunks_per_row) == (ODD, 8, 4)
     # other odd starts take the element path
-    assert plan(lib, start=3, end=11).path == 2                      # element 3 of its vector
+    assert plan(lib, start=3, end=11).path == 2                      # element 3 of 8 and of 4
     assert plan(lib, start=1, end=9, x=BASE + 4).path == 2           # x only 4-byte aligned
     assert plan(lib, shape=(2, 4, 3, 18), start=1, end=9).path == 2  # 36-byte rows
     assert plan(lib, start=1, end=9, x=BASE + 2).path == 2           # x only 2-byte aligned
     assert plan(lib, start=1, end=9, r1=BASE + 2**30 + 2).path == 2  # cos only 2-byte aligned
-    assert plan(lib, dtype=FP32, start=3, end=11).path == 2          # fp32, element 3
     assert plan(lib, dtype=FP32, start=1, end=9, x=BASE + 4).path == 2   # fp32 needs 8 bytes
     assert plan(lib, start=2, end=10).vec_bytes == 4                 # 4-byte slice offset
     assert plan(lib, x=BASE + 8).vec_bytes == 8                      # x only 8-byte aligned

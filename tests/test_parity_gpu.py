@@ -65,8 +65,9 @@ def test_sweep(dtype, k):
 ODD_STARTS = [
     # shape, start, end, broadcast form, x's element offset in its buffer.
     # An odd start at element 1 of an aligned 16- or 8-byte vector of x runs
-    # a lane per vector (path 4), any other odd start the element path (path
-    # 2); odd_path() below states the rule.  Cases: the last lane storing part
+    # a lane per vector (path 4; fp32 rows take any odd start at 8 bytes),
+    # any other odd start the element path (path 2); odd_path() below states
+    # the rule.  Cases: the last lane storing part
     # of its vector, the slice ending one element before the row's end, idle
     # head slots, cos/sin per head, one pair per row, rows whose lanes
     # straddle two warps, and x aligned to 16, 8 or 4 bytes only.
@@ -92,13 +93,13 @@ ODD_STARTS = [
 
 
 def odd_path(shape, start, off, dtype):
-    """4 when the slice starts at element 1 of the widest 16- or 8-byte
-    vector that divides x's address (buffer base + off elements) and its row
-    pitch, else 2."""
+    """4 when some 16- or 8-byte vector that divides x's address (buffer base
+    + off elements) and its row pitch puts the start at element 1 of a
+    vector, else 2."""
     e = synth.ELEM_BYTES[dtype]
     for v in (16, 8):
-        if (off * e) % v == 0 and (shape[3] * e) % v == 0:
-            return 4 if start % (v // e) == 1 else 2
+        if (off * e) % v == 0 and (shape[3] * e) % v == 0 and start % (v // e) == 1:
+            return 4
     return 2
 
 
