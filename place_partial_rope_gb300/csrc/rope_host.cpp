@@ -163,10 +163,10 @@ rope_status_t check(const void* x, const void* r1, const void* r2, int dtype, in
 // ran those 8 % faster there and level after an L2 flush.)
 // The odd-start kernel (a lane per aligned vector of x, vec bytes): 4 heads
 // per thread on 16-byte vectors (the most that kernel instance allows), 8
-// on 8-byte ones.  Back to back on GB300: GQA [1, 65) 16-byte 58.0 us (U
-// = 4) against 64.0 (2); 8-byte 60.0 (8) against 68.1 (4); large fp32
-// [1, 65) 16-byte 98.8 (4) against 113.8 (2), 8-byte 106.0 (8) against
-// 127.0 (4).
+// on 8-byte ones.  Back to back on GB300: GQA [9, 73) 16-byte 56.9 us (U
+// = 4) against 60.7 (2); [5, 69) 8-byte 58.3 (8) against 64.8 (4); large
+// fp32 [1, 65) 16-byte 98.8 (4) against 113.8 (2), [3, 67) 8-byte 102.9
+// (8) against 118.0 (4).
 int odd_heads_cap(int e, int vec) {
     (void)e;
     return vec == 16 ? 4 : 8;
