@@ -773,15 +773,16 @@ rope_status_t rope_partial_plan_mode(const void* x, const void* r1, const void* 
     g_msg[0] = '\0';
     if (!plan) return fail(ROPE_ERR_NULLPTR, "plan is null");
     *plan = rope_plan_t{};
-    if (mode != kInterleave && mode != kHalf)
-        return fail(ROPE_ERR_INVALID, "rotary mode %d is not interleave (1) or half (2)", (int)mode);
+    const int m = static_cast<int>(mode);
+    if (m != kInterleave && m != kHalf)
+        return fail(ROPE_ERR_INVALID, "rotary mode %d is not interleave (1) or half (2)", m);
     Resolved R;
     rope_status_t st = check(x, r1, r2, dtype, B, S, N, D, r1_shape, r1_stride, r2_shape,
                              r2_stride, start, end, &R);
     if (st != ROPE_OK || R.empty) return st;
     Plan P;
     const Seg seg{const_cast<void*>(x), N, D, start};
-    st = make_plan(kFwd, mode, dtype, &seg, 1, r1, r2, R, &P);
+    st = make_plan(kFwd, m, dtype, &seg, 1, r1, r2, R, &P);
     if (st != ROPE_OK) return st;
     if (!kernel_lookup(P))
         return fail(ROPE_ERR_CUDA, "internal error: no kernel instance for this plan");

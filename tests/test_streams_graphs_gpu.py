@@ -6,7 +6,7 @@ import pytest
 import torch
 
 import oracle
-from gpu_util import DEV, assert_same, to_dev
+from gpu_util import assert_same, to_dev
 from place_partial_rope_gb300 import binding, synth
 
 pytestmark = pytest.mark.gpu
