@@ -470,27 +470,26 @@ __device__ __forceinline__ void rope_body(const KernelArgs& a) {
                     store_x_half<T, W, SCALAR>(xp[i] + ho, yb);
                 }
             }
-            continue;
-        }
-
-        Words<W> xv[U];
+        } else {
+            Words<W> xv[U];
 #pragma unroll
-        for (int i = 0; i < U; ++i)
-            if (i == 0 || n0 + i < nheads) xv[i] = load_x<T, W, SCALAR>(xp[i]);
+            for (int i = 0; i < U; ++i)
+                if (i == 0 || n0 + i < nheads) xv[i] = load_x<T, W, SCALAR>(xp[i]);
 
-        Words<W> cv, sv;
-        if constexpr (!RHEAD) {
-            cv = load_r<T, W, SCALAR>(c_p);
-            sv = load_r<T, W, SCALAR>(s_p);
-        }
+            Words<W> cv, sv;
+            if constexpr (!RHEAD) {
+                cv = load_r<T, W, SCALAR>(c_p);
+                sv = load_r<T, W, SCALAR>(s_p);
+            }
 #pragma unroll
-        for (int i = 0; i < U; ++i) {
-            if (i == 0 || n0 + i < nheads) {
-                if constexpr (RHEAD) {
-                    cv = load_r<T, W, SCALAR>(c_p + int64_t(i) * a.r1_n);
-                    sv = load_r<T, W, SCALAR>(s_p + int64_t(i) * a.r2_n);
+            for (int i = 0; i < U; ++i) {
+                if (i == 0 || n0 + i < nheads) {
+                    if constexpr (RHEAD) {
+                        cv = load_r<T, W, SCALAR>(c_p + int64_t(i) * a.r1_n);
+                        sv = load_r<T, W, SCALAR>(s_p + int64_t(i) * a.r2_n);
+                    }
+                    store_x<T, W, SCALAR>(xp[i], rotate_chunk<T, W, DIR>(xv[i], cv, sv));
                 }
-                store_x<T, W, SCALAR>(xp[i], rotate_chunk<T, W, DIR>(xv[i], cv, sv));
             }
         }
     }
