@@ -3,9 +3,10 @@
 Bar: bit-exact for bf16, fp16 and fp32 (both sides compute each product and
 sum as one fp32 rounding and round once to the storage type), including
 every byte outside [start, end).  NaN matches NaN.  The five named workloads
-run at full size and are compared on every element; a sweep of small seeded
-cases covers every dtype, broadcast form, aligned / unaligned / odd slice,
-ragged head counts and the degenerate shapes.
+and the odd-start cases the benchmark times run at full size and are
+compared on every element; a sweep of small seeded cases covers every dtype,
+broadcast form, aligned / unaligned / odd slice, ragged head counts and the
+degenerate shapes.
 """
 import numpy as np
 import pytest
@@ -131,6 +132,29 @@ def test_odd_starts(dtype, k):
                     dtype, f"{shape} [{st},{en}) {form} offset {off} {direction}")
         assert np.array_equal(host[:lo], canary[:lo]), "canary before x changed"
         assert np.array_equal(host[lo + n:], canary[lo + n:]), "canary after x changed"
+
+
+# The odd-start cases bench.py times, at full size and with its inputs: the
+# gqa shape (fp16, one cos/sin row per position) and the large fp32 shape
+# (per-batch position offsets), each with the path and vector width the
+# planner picks; every element compared, forward and backward.
+ODD_FULL = [("gqa", 1, 65, 4, 16), ("gqa", 1, 63, 4, 16), ("gqa", 5, 69, 4, 8), ("gqa", 3, 45, 2, 4),
+            ("large_unaligned", 1, 65, 4, 16), ("large_unaligned", 3, 67, 4, 8)]
+
+
+@pytest.mark.parametrize("name,st,en,path,vec", ODD_FULL)
+def test_odd_start_full_size(name, st, en, path, vec):
+    w = synth.WORKLOADS[name]
+    x = synth.normal(w.shape, w.dtype, w.seed)
+    r1, r2 = synth.rope_table(synth.positions(w), en - st, w.dtype)
+    xd, c, s = to_dev(x, w.dtype), to_dev(r1, w.dtype), to_dev(r2, w.dtype)
+    plan = binding.rope_partial_plan(xd, c, s, st, en)
+    assert (plan.path, plan.vec_bytes) == (path, vec)
+    del xd, c, s
+    for direction in ("fwd", "bwd"):
+        got = run_cuda(direction, x, r1, r2, w.dtype, st, en)
+        assert_same(got, run_oracle(direction, x, r1, r2, w.dtype, st, en), w.dtype,
+                    f"{name} [{st},{en}) {direction}")
 
 
 @pytest.mark.parametrize("dtype", ["bf16", "fp16", "fp32"])
