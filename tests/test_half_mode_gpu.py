@@ -61,18 +61,22 @@ def test_half_sweep(dtype, k):
                     f"half {shape} [{st},{en}) {form} {direction}")
 
 
-@pytest.mark.parametrize("name", ["gqa", "large_unaligned"])
-def test_half_named_shapes_full_size(name):
+@pytest.mark.parametrize("name,span", [("gqa", None), ("large_unaligned", None),
+                                       ("large_unaligned", (0, 96))])
+def test_half_named_shapes_full_size(name, span):
     """The gqa and large fp32 shapes in half-split mode with a half-layout
-    cos/sin table, forward and backward, every element."""
+    cos/sin table, forward and backward, every element; the large shape also
+    at [0, 96), whose 12 accesses per half run both halves in one thread
+    (the benchmark's half-split cases)."""
     w = synth.WORKLOADS[name]
+    st, en = span if span else (w.start, w.end)
     x = synth.normal(w.shape, w.dtype, w.seed)
     g = synth.normal(w.shape, w.dtype, w.seed + 500)
-    r1, r2 = synth.rope_table(synth.positions(w), w.L, w.dtype, layout="half")
+    r1, r2 = synth.rope_table(synth.positions(w), en - st, w.dtype, layout="half")
     for direction, inp in (("fwd", x), ("bwd", g)):
-        got = run_half(direction, inp, r1, r2, w.dtype, w.start, w.end)
-        assert_same(got, oracle_half(direction, inp, r1, r2, w.dtype, w.start, w.end), w.dtype,
-                    f"half {name} {direction}")
+        got = run_half(direction, inp, r1, r2, w.dtype, st, en)
+        assert_same(got, oracle_half(direction, inp, r1, r2, w.dtype, st, en), w.dtype,
+                    f"half {name} [{st},{en}) {direction}")
 
 
 @pytest.mark.parametrize("dtype", ["bf16", "fp32"])

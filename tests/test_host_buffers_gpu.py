@@ -54,11 +54,18 @@ def test_host_x_with_device_tables():
     assert_same(got, run_oracle("fwd", x, r1, r2, "bf16", 8, 40), "bf16", "host x, device cos/sin")
 
 
-def test_named_workload_on_host_buffers():
-    w = synth.WORKLOADS["gqa"]
+@pytest.mark.parametrize("name,direction", [("gqa", "bwd"), ("large_unaligned", "fwd"),
+                                            ("large_unaligned", "bwd")])
+def test_named_workload_on_host_buffers(name, direction):
+    """Full size on page-locked host buffers, every element: the gqa shape
+    and the large fp32 shape, whose calls the benchmark's end-to-end figure
+    times."""
+    w = synth.WORKLOADS[name]
     x, r1, r2, g = synth.workload_inputs(w)
-    got = run_host("bwd", g, r1, r2, w.dtype, w.start, w.end)
-    assert_same(got, run_oracle("bwd", g, r1, r2, w.dtype, w.start, w.end), w.dtype, "gqa bwd host")
+    inp = x if direction == "fwd" else g
+    got = run_host(direction, inp, r1, r2, w.dtype, w.start, w.end)
+    assert_same(got, run_oracle(direction, inp, r1, r2, w.dtype, w.start, w.end), w.dtype,
+                f"{name} {direction} host")
 
 
 def test_pageable_host_memory_is_used_or_refused():
