@@ -138,8 +138,10 @@ struct Pack<__half> {
 };
 
 // ------------------------------------------------------------------------
-// global memory: x (read then written by the same thread) and cos/sin
-// (read-only for the whole kernel, so they may take the non-coherent path)
+// global memory: x (each byte read and then written by the same thread,
+// except in the odd-start kernel, whose lanes also read a neighbour's edge
+// word that they never write) and cos/sin (read-only for the whole kernel,
+// so they may take the non-coherent path)
 // ------------------------------------------------------------------------
 
 // x loads carry an explicit 64-byte L2 prefetch size.  Without it a miss
